@@ -1,0 +1,470 @@
+#!/usr/bin/env python
+"""Selective-scan bench: scanned elements per second (Bsz*Dch*L) of one
+training-and-decode pass of the whole hot path on one workload.
+
+One step = ss_scan_fwd (discretise, scan, contract, skip, gate) +
+ss_scan_bwd (its three stages: segment states, reverse pass, reduction) +
+one ss_step decode token continuing from the forward's final state (+ for
+N > 1 the all-reduce of dA, dD, ddelta_bias across replicas).
+
+Workload: the Mamba-130M-shaped layer Bsz=8, Dch=1536, L=2048, N=16 with bf16
+inputs/outputs and float32 state and accumulation; synthetic seeded data
+(u, z, B, C, delta_raw, dy ~ N(0,1); A[d,n] = -(n+1); D ~ N(0,1); delta_bias
+= inverse softplus of dt, dt log-uniform in [1e-3, 1e-1]).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line on rank 0.  ``--impl reference`` times the fp64 CPU
+oracle (the method as plain sequential code) on a bounded sample of the same
+workload on this machine's host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "selective-scan Gelem/s (B·D·L), fwd and fwd+bwd; % of HBM/MUFU roofline"
+UNIT = "Gelem/s"
+CFG_INDEX = 1
+N_STATE = 16
+
+# Hardware figures for the roofline denominators.
+SMS = 148
+SM_MAX_MHZ = 2032.0
+FP32_LANES = 128            # FP32 ops per clock per SM (one per lane)
+ALU_PEAK_TOPS = SMS * FP32_LANES * SM_MAX_MHZ * 1e6 / 1e12   # 38.49 T ops/s
+L2_BYTES = 126 * 2 ** 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6400.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic work per scanned element (b, d, t) of each kernel, N = 16,
+# s = bytes per I/O element, Dch = channels.  "ops" counts FP32 and MUFU
+# operations (one issue slot each); bytes count each tensor read or written
+# once.
+#   fwd:         MUFU N+4 (N decays, softplus 2, sigmoid 2); FP32 4N+10
+#                (per state: delta*A, delta*u*B, state FMA, output FMA).
+#                bytes 4s + 2Ns/Dch (u, delta, z in; y out; B, C per (b,t)).
+#   bwd_states:  MUFU N+2; FP32 3N+5 (decay argument, input term, fold FMA).
+#                bytes 2s + 4 + Ns/Dch (u, delta in; one f32 state per
+#                16 steps and state out).
+#   bwd_reverse: MUFU N+6; FP32 14N+20 (decay arg, state replay 2, output
+#                for dz, adjoint 2, dC, dB, du-sum, ddelta-sum 2, dA, the
+#                two row sums of dB and dC).
+#                bytes 7s + 4 + 2Ns/Dch (u, delta, z, dy, states in;
+#                du, ddelta, dz out; B, C per (b,t)).
+#   bwd_reduce:  bytes 2N*4*(G+1)/Dch per element (G = Dch/16 partials of
+#                dB, dC read, dB, dC written); no arithmetic to speak of.
+#   step:        per (b,d) row: bytes 8N + 4s; MUFU N+4; FP32 4N+10.
+# ---------------------------------------------------------------------------
+def kernel_work(s, Dch, N=N_STATE):
+    G = (Dch + 15) // 16
+    return {
+        "fwd": dict(ops=(N + 4) + (4 * N + 10), bytes=4 * s + 2 * N * s / Dch),
+        "bwd_states": dict(ops=(N + 2) + (3 * N + 5), bytes=2 * s + 4 + N * s / Dch),
+        "bwd_reverse": dict(ops=(N + 6) + (14 * N + 20), bytes=7 * s + 4 + 2 * N * s / Dch),
+        "bwd_reduce": dict(ops=0, bytes=2 * N * 4 * (G + 1) / Dch),
+    }
+
+
+def roofline(name, work, elems, ms, hbm_gbs, traffic=None):
+    t = ms * 1e-3
+    t_alu = work["ops"] * elems / (ALU_PEAK_TOPS * 1e12)
+    t_hbm = work["bytes"] * elems / (hbm_gbs * 1e9)
+    if t_alu >= t_hbm:
+        ach = work["ops"] * elems / t / 1e12
+        return {"kernel": name, "bound": "alu", "achieved": round(ach, 3),
+                "peak": round(ALU_PEAK_TOPS, 2), "unit": "TOP/s", "frac": round(ach / ALU_PEAK_TOPS, 4),
+                "traffic": traffic, "algorithmic_ops": work["ops"] * elems,
+                "algorithmic_bytes": work["bytes"] * elems}
+    ach = work["bytes"] * elems / t / 1e9
+    return {"kernel": name, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_gbs,
+            "unit": "GB/s", "frac": round(ach / hbm_gbs, 4), "traffic": traffic,
+            "algorithmic_ops": work["ops"] * elems, "algorithmic_bytes": work["bytes"] * elems}
+
+
+def csrc_digest():
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "selective_state_space_114_b300", "csrc", "*"))):
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, when it was
+    taken on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        d = json.load(open(p))
+    except Exception:
+        return None
+    if d.get("csrc_digest") != csrc_digest():
+        return None
+    v = d.get("kernels", {}).get(kernel)
+    return None if v is None else v.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    def __init__(self, device_index=0):
+        self.samples = []
+        self._stop = threading.Event()
+        self.ok = False
+        try:
+            import pynvml as nv
+            nv.nvmlInit()
+            self.nv = nv
+            handle = None
+            try:
+                import torch
+                props = torch.cuda.get_device_properties(device_index)
+                bus = "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id,
+                                            props.pci_device_id)
+                handle = nv.nvmlDeviceGetHandleByPciBusId(bus.encode())
+            except Exception:
+                handle = None
+            if handle is None:
+                handle = nv.nvmlDeviceGetHandleByIndex(device_index)
+            self.h = handle
+            self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(handle, nv.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception as e:  # no NVML: report what we could not sample
+            self.err = str(e)
+
+    def _reasons(self):
+        nv = self.nv
+        try:
+            return nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+        except Exception:
+            return nv.nvmlDeviceGetCurrentClocksThrottleReasons(self.h)
+
+    def _run(self):
+        nv = self.nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append((nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM),
+                                     int(self._reasons())))
+            except Exception:
+                pass
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        names = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+                 0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+                 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+                 0x100: "display_clock_setting"}
+        busy = [s for s in self.samples if not (s[1] & 0x1)] or self.samples
+        seen = set()
+        for _, r in busy:
+            for bit, nm in names.items():
+                if r & bit:
+                    seen.add(nm)
+        mhz = statistics.median([s[0] for s in busy]) if busy else None
+        return {"sm_mhz": mhz, "sm_max_mhz": self.max_mhz, "reasons": sorted(seen),
+                "samples": len(busy)}
+
+
+# ---------------------------------------------------------------------------
+# distributed set-up
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def workload_config(world):
+    cfg = synth.config(CFG_INDEX)
+    E = cfg["Bsz"] * cfg["Dch"] * cfg["L"]
+    per_step_mb = (8 * E * 2 + 8 * E * 2) / 2 ** 20
+    return cfg, {
+        "workload": "mamba130m-shaped selective-scan layer: Bsz=8 Dch=1536 L=2048 N=16, bf16 "
+                    "I/O, f32 state; step = fwd + bwd (3 stages) + 1 decode token",
+        "Bsz": cfg["Bsz"], "Dch": cfg["Dch"], "L": cfg["L"], "N": cfg["N"], "io_dtype": "bf16",
+        "softplus": True, "gate": True, "global_batch": cfg["Bsz"] * world,
+        "parallelism": "replicas" if world == 1 else f"dp{world} (param-grad all-reduce)",
+        "l2": f"inputs larger than L2: ~{per_step_mb:.0f} MiB of activations and gradients "
+              f"touched per step vs {L2_BYTES // 2**20} MiB L2; no flush",
+    }
+
+
+# ---------------------------------------------------------------------------
+# CPU (oracle) timing
+# ---------------------------------------------------------------------------
+def oracle_sample_step(cfg, nch, seed):
+    """One fp64 oracle pass (fwd + bwd + one step) over all Bsz batches of
+    the first ``nch`` channels, L = full length.  Returns seconds."""
+    import oracle
+    sub = dict(cfg, Dch=nch)
+    x = synth.make_inputs(sub, seed=seed, with_dy=True)
+    w = {k: synth.widen(v) for k, v in x.items()}
+    t0 = time.perf_counter()
+    _, h = oracle.scan_fwd(w["u"], w["delta"], w["A"], w["B"], w["C"], w["D"], w["z"],
+                           w["delta_bias"], True)
+    oracle.scan_bwd(w["u"], w["delta"], w["A"], w["B"], w["C"], w["D"], w["z"],
+                    w["delta_bias"], True, w["dy"])
+    tok = synth.step_inputs(dict(sub, L=1), 0, seed=seed)
+    tw = {k: synth.widen(v) for k, v in tok.items()}
+    oracle.step(h, tw["u"], tw["delta"], w["A"], tw["B"], tw["C"], w["D"], tw["z"],
+                w["delta_bias"], True)
+    return time.perf_counter() - t0
+
+
+def size_oracle_sample(cfg, target_s, seed):
+    cores = os.cpu_count() or 1
+    n0 = max(2, min(cores, 8))
+    t = oracle_sample_step(cfg, n0, seed)
+    per_ch = t / n0
+    n = int(max(n0, min(cfg["Dch"], target_s / max(per_ch, 1e-9))))
+    return n
+
+
+def cpu_baseline(cfg, seed, target_s=12.0):
+    import oracle
+    cores = oracle.default_threads()
+    n = size_oracle_sample(cfg, target_s, seed)
+    t = oracle_sample_step(cfg, n, seed)
+    elems = cfg["Bsz"] * n * cfg["L"]
+    return {"value": round(elems / t / 1e9, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"fp64 oracle fwd+bwd+1 step over all {cfg['Bsz']} batches x first {n} of "
+                      f"{cfg['Dch']} channels x L={cfg['L']} ({elems} elements, {t:.1f} s)"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    cfg, conf = workload_config(1)
+    if rank != 0:
+        return 0
+    import oracle
+    cores = oracle.default_threads()
+    W, K = max(3, args.warmup), args.steps
+    budget = 150.0  # seconds for the whole run
+    per_step = max(0.5, budget / (W + K))
+    n = size_oracle_sample(cfg, per_step, cfg["seed"])
+    for _ in range(W):
+        oracle_sample_step(cfg, n, cfg["seed"])
+    times = [oracle_sample_step(cfg, n, cfg["seed"]) for _ in range(K)]
+    elems = cfg["Bsz"] * n * cfg["L"]
+    ms = 1e3 * sum(times) / K
+    value = elems / (ms * 1e-3) / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": K, "warmup": W, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": conf,
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"each step: fp64 oracle fwd+bwd+1 decode step over all "
+                                   f"{cfg['Bsz']} batches x first {n} of {cfg['Dch']} channels x "
+                                   f"L={cfg['L']} ({elems} elements)"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU timing
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_env()
+    if args.gpus != world:
+        if world == 1 and args.gpus > 1:
+            raise SystemExit("bench.py --gpus N>1 must be launched with torch.distributed.run")
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import selective_state_space_114_b300 as ss
+    from selective_state_space_114_b300 import dist as sdist
+
+    dev = torch.device("cuda", local)
+    cfg, conf = workload_config(world)
+    seed = sdist.rank_seed(cfg["seed"], rank)
+    Bsz, Dch, L, N = cfg["Bsz"], cfg["Dch"], cfg["L"], cfg["N"]
+    E = Bsz * Dch * L
+    W, K = max(3, args.warmup), args.steps
+
+    x = synth.make_inputs(cfg, seed=seed, with_dy=True)
+    tok = synth.step_inputs(dict(cfg, L=1), 0, seed=seed)
+
+    def host(a, pin=True):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if a.dtype == np.uint16:
+            t = t.view(torch.bfloat16)
+        return t.pin_memory() if pin else t
+
+    hx = {k: host(v) for k, v in x.items()}
+    ht = {k: host(v) for k, v in tok.items()}
+    d = {k: v.to(dev) for k, v in hx.items()}
+    dt = {k: v.to(dev) for k, v in ht.items()}
+    bf = torch.bfloat16
+    y = torch.empty((Bsz, Dch, L), device=dev, dtype=bf)
+    h = torch.empty((Bsz, Dch, N), device=dev, dtype=torch.float32)
+    g = {"du": torch.empty_like(y), "ddelta": torch.empty_like(y), "dz": torch.empty_like(y),
+         "dA": torch.empty((Dch, N), device=dev), "dB": torch.empty((Bsz, N, L), device=dev),
+         "dC": torch.empty((Bsz, N, L), device=dev), "dD": torch.empty((Dch,), device=dev),
+         "ddelta_bias": torch.empty((Dch,), device=dev)}
+    ws = torch.empty(ss.ss_scan_bwd_workspace_size(Bsz, Dch, L, N, ss.SS_BF16), device=dev,
+                     dtype=torch.uint8)
+    yt = torch.empty((Bsz, Dch), device=dev, dtype=bf)
+    stages = ("ss_scan_bwd_states", "ss_scan_bwd_reverse", "ss_scan_bwd_reduce")
+    names = ["fwd", "bwd_states", "bwd_reverse", "bwd_reduce", "step"]
+
+    def one_step(evs=None, src=None):
+        if src is not None:  # e2e: this step's inputs arrive from pinned host memory
+            for k, v in src[0].items():
+                d[k].copy_(v, non_blocking=True)
+            for k, v in src[1].items():
+                dt[k].copy_(v, non_blocking=True)
+        rec = (lambda i: evs[i].record()) if evs is not None else (lambda i: None)
+        rec(0)
+        ss.ss_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                       d["delta_bias"], True, return_last_state=True, out=y, h_last=h)
+        rec(1)
+        for i, st in enumerate(stages):
+            ss.ss_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                           d["delta_bias"], True, d["dy"], workspace=ws, out=g, stages=(st,))
+            rec(2 + i)
+        ss.ss_step(h, dt["u"], dt["delta"], d["A"], dt["B"], dt["C"], d["D"], dt["z"],
+                   d["delta_bias"], True, out=yt)
+        rec(5)
+        if world > 1:
+            sdist.allreduce_param_grads(g)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(W):
+        one_step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record()
+        for k in range(K):
+            one_step(evs[k])
+        end.record()
+        torch.cuda.synchronize()
+    barrier()
+    ms_local = start.elapsed_time(end) / K
+    ms = sdist.max_over_ranks(ms_local, device=dev)
+    per_kernel = {nm: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K))
+                  for i, nm in enumerate(names)}
+    value = world * E / (ms * 1e-3) / 1e9
+    fwd_gelem = E / (per_kernel["fwd"] * 1e-3) / 1e9
+
+    # end to end through the public API with host buffers
+    Ke = max(3, min(K, 10))
+    outs = {"y": y, "yt": yt, **g}
+    hout = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+    h2d = sum(v.numel() * v.element_size() for v in list(hx.values()) + list(ht.values()))
+    d2h = sum(v.numel() * v.element_size() for v in outs.values())
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(Ke):
+        one_step(src=(hx, ht))
+        for k, v in outs.items():
+            hout[k].copy_(v, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = sdist.max_over_ranks(e0.elapsed_time(e1) / Ke, device=dev)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    hbm, peak_src = load_peaks()
+    work = kernel_work(2, Dch)
+    roofs = {nm: roofline(nm, work[nm], E, per_kernel[nm], hbm, ncu_traffic(nm))
+             for nm in names if nm in work}
+    dominant = max(roofs, key=lambda nm: per_kernel[nm])
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": conf,
+        "fwd_gelem_s": round(fwd_gelem, 3),
+        "roofline": roofs[dominant],
+        "roofline_peak_source": f"alu: {SMS} SMs x {FP32_LANES} FP32 ops/clk x {SM_MAX_MHZ} MHz; "
+                                f"hbm: {hbm} GB/s {peak_src}",
+        "kernels": {nm: {"ms": round(per_kernel[nm], 4),
+                         "share": round(per_kernel[nm] / sum(per_kernel.values()), 4),
+                         **({"frac": roofs[nm]["frac"], "bound": roofs[nm]["bound"]}
+                            if nm in roofs else {})} for nm in names},
+        "gpu_launches": K * 6,
+        "e2e": {"value": round(world * E / (e2e_ms * 1e-3) / 1e9, 3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 3)},
+        "clocks": clk.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, seed)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle timing on the host cores")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

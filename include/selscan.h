@@ -1,0 +1,175 @@
+/*
+ * selscan.h -- C ABI of libselscan, the selective scan of the Mamba
+ * selective state-space layer on NVIDIA B300 (sm_103a).
+ *
+ * The operation (per batch b, channel d, state n; time t = 0 .. L-1):
+ *
+ *   delta_t  = softplus(delta_raw_t + delta_bias_d)   (raw sum if softplus == 0)
+ *   h_t[n]   = exp(delta_t * A_d[n]) * h_{t-1}[n] + delta_t * B_t[n] * u_t,  h_{-1} = 0
+ *   y_t      = (sum_n C_t[n] * h_t[n] + D_d * u_t) * silu(z_t)
+ *
+ * Where it comes from: the selective SSM layer of Mamba ("Mamba SSM 架构",
+ * toolpotion.ai: the layer of section 3 / algorithm 2 of the Mamba paper;
+ * "Mamba 7.9.1", lpnh.cn, section 2.2: the SSM parameters become functions
+ * of the input), evaluated as the sequential recurrence quoted in the
+ * "PyTorch 한 파일에서의 Mamba 구현" thread (news.hada.io, topic 12448: the
+ * state update with deltaA and deltaB_u, then the contraction with C over
+ * the state dimension).  The pages name deltaA and deltaB_u but do not print
+ * them; this library reads them as exp(delta*A) and delta*B*u.  The fused,
+ * "hardware-aware" evaluation (state kept on chip, backward by recomputation)
+ * is described on the "mamba.py" page (gittoolsai.com), performance section.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library allocates no memory and keeps no state between calls.
+ *   - Layouts are row-major with time innermost (no strides):
+ *       u, delta, z, y, du, ddelta, dz, dy : [Bsz][Dch][L]   (I/O dtype)
+ *       B, C                               : [Bsz][N][L]     (I/O dtype)
+ *       dB, dC                             : [Bsz][N][L]     float32
+ *       A, dA                              : [Dch][N]        float32
+ *       D, delta_bias, dD, ddelta_bias     : [Dch]           float32
+ *       h, h_last                          : [Bsz][Dch][N]   float32
+ *     The I/O dtype (ss_dtype) is float32 or bf16 (uint16 bit patterns);
+ *     arithmetic is float32 throughout, the state h is always float32.
+ *   - Every pointer must be 16-byte aligned (SS_ERR_ALIGN otherwise).  Any
+ *     L >= 0 is accepted; rows whose byte length is a multiple of 16 take the
+ *     vectorised path, other L a slower element-wise path.
+ *   - Optional inputs: D == NULL means D = 0, z == NULL means no gate,
+ *     delta_bias == NULL means a zero bias.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  Arguments are checked before anything is launched; a
+ *     rejected call launches nothing and writes nothing.  SS_ERR_CUDA reports
+ *     a launch error (cudaGetLastError after the launch); faults during
+ *     execution surface at the caller's next synchronisation.
+ *   - Outputs are overwritten, never accumulated into.
+ *   - N (the state size, d_state) must be 16.
+ */
+#ifndef SELSCAN_H_
+#define SELSCAN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* ss_stream_t;
+
+typedef enum { SS_F32 = 0, SS_BF16 = 1 } ss_dtype;
+
+typedef enum {
+    SS_OK = 0,
+    SS_ERR_NULL = 1,           /* a required pointer is NULL                      */
+    SS_ERR_SHAPE = 2,          /* negative or too-large size                      */
+    SS_ERR_DTYPE = 3,          /* unknown ss_dtype                                */
+    SS_ERR_N_UNSUPPORTED = 4,  /* N != 16                                         */
+    SS_ERR_ALIGN = 5,          /* a pointer is not 16-byte aligned                */
+    SS_ERR_WORKSPACE = 6,      /* workspace NULL/misaligned or smaller than needed */
+    SS_ERR_CUDA = 7            /* the CUDA runtime reported a launch error        */
+} ss_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* ss_status_str(ss_status s);
+
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+int ss_version(void);
+
+/*
+ * Forward selective scan.
+ *   in : u, delta (delta_raw), z [Bsz][Dch][L]; B, C [Bsz][N][L]; A [Dch][N];
+ *        D, delta_bias [Dch] (nullable, as are z); softplus: 0 or 1.
+ *   out: y [Bsz][Dch][L] (I/O dtype);
+ *        h_last [Bsz][Dch][N] float32 (nullable): the state after the last
+ *        step (zeros when L == 0), to hand a sequence over to ss_step.
+ * Zero-sized Bsz, Dch or L are valid (nothing but h_last is written).
+ */
+ss_status ss_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
+                      const void* C, const float* D, const void* z, const float* delta_bias,
+                      int softplus, int64_t Bsz, int64_t Dch, int64_t L, int64_t N,
+                      ss_dtype dtype, void* y, float* h_last, ss_stream_t stream);
+
+/*
+ * Bytes of device workspace ss_scan_bwd needs for these sizes (written to
+ * *bytes; 0 is possible).  Pure host computation, no CUDA call.
+ */
+ss_status ss_scan_bwd_workspace_size(int64_t Bsz, int64_t Dch, int64_t L, int64_t N,
+                                     ss_dtype dtype, size_t* bytes);
+
+/*
+ * Backward of ss_scan_fwd (zero initial state) for an upstream gradient dy
+ * of y.  The state trajectory is recomputed, not stored: the workspace holds
+ * the states at 16-step segment boundaries and per-block partial sums of
+ * dA, dB, dC, dD and ddelta_bias, reduced in a fixed order, so reruns are
+ * bitwise identical.
+ *   in : the forward's inputs, dy [Bsz][Dch][L] (I/O dtype),
+ *        workspace (device, 16-byte aligned, >= ss_scan_bwd_workspace_size).
+ *   out: du, ddelta (gradient of delta_raw), dz [Bsz][Dch][L] in the I/O
+ *        dtype; dA [Dch][N], dB and dC [Bsz][N][L], dD and ddelta_bias
+ *        [Dch] in float32.  dD / dz / ddelta_bias must be non-NULL exactly
+ *        when D / z / delta_bias are.
+ * The workspace contents on return are unspecified.
+ */
+ss_status ss_scan_bwd(const void* u, const void* delta, const float* A, const void* B,
+                      const void* C, const float* D, const void* z, const float* delta_bias,
+                      int softplus, const void* dy, int64_t Bsz, int64_t Dch, int64_t L,
+                      int64_t N, ss_dtype dtype, void* du, void* ddelta, float* dA, float* dB,
+                      float* dC, float* dD, void* dz, float* ddelta_bias, void* workspace,
+                      size_t workspace_bytes, ss_stream_t stream);
+
+/*
+ * The three stages ss_scan_bwd runs, in this order, exposed for callers that
+ * time them separately or interleave other work between them.  Each takes
+ * exactly ss_scan_bwd's arguments and performs the same checks; calling the
+ * three in order on one stream (same arguments, same workspace) is
+ * ss_scan_bwd.
+ *   ss_scan_bwd_states : recomputes the forward states at every 16-step
+ *                        segment boundary into the workspace.
+ *   ss_scan_bwd_reverse: the reverse-time pass; writes du, ddelta, dz and
+ *                        the per-block partial sums of dA, dB, dC, dD,
+ *                        ddelta_bias into the workspace.
+ *   ss_scan_bwd_reduce : sums the partials in a fixed order into dA, dB,
+ *                        dC, dD, ddelta_bias.
+ */
+ss_status ss_scan_bwd_states(const void* u, const void* delta, const float* A, const void* B,
+                             const void* C, const float* D, const void* z,
+                             const float* delta_bias, int softplus, const void* dy, int64_t Bsz,
+                             int64_t Dch, int64_t L, int64_t N, ss_dtype dtype, void* du,
+                             void* ddelta, float* dA, float* dB, float* dC, float* dD, void* dz,
+                             float* ddelta_bias, void* workspace, size_t workspace_bytes,
+                             ss_stream_t stream);
+ss_status ss_scan_bwd_reverse(const void* u, const void* delta, const float* A, const void* B,
+                              const void* C, const float* D, const void* z,
+                              const float* delta_bias, int softplus, const void* dy,
+                              int64_t Bsz, int64_t Dch, int64_t L, int64_t N, ss_dtype dtype,
+                              void* du, void* ddelta, float* dA, float* dB, float* dC,
+                              float* dD, void* dz, float* ddelta_bias, void* workspace,
+                              size_t workspace_bytes, ss_stream_t stream);
+ss_status ss_scan_bwd_reduce(const void* u, const void* delta, const float* A, const void* B,
+                             const void* C, const float* D, const void* z,
+                             const float* delta_bias, int softplus, const void* dy, int64_t Bsz,
+                             int64_t Dch, int64_t L, int64_t N, ss_dtype dtype, void* du,
+                             void* ddelta, float* dA, float* dB, float* dC, float* dD, void* dz,
+                             float* ddelta_bias, void* workspace, size_t workspace_bytes,
+                             ss_stream_t stream);
+
+/*
+ * One recurrent step (the "RNN form" used for token-by-token decoding;
+ * "mamba.py" page, step function; "Mamba 7.9.1", section 6.2):
+ *   in/out: h [Bsz][Dch][N] float32, updated in place;
+ *   in : u_t, delta_t, z_t [Bsz][Dch]; B_t, C_t [Bsz][N] (I/O dtype);
+ *        A [Dch][N]; D, delta_bias [Dch] (nullable, as is z_t).
+ *   out: y_t [Bsz][Dch] (I/O dtype).
+ * h must not alias any other argument.
+ */
+ss_status ss_step(float* h, const void* u_t, const void* delta_t, const float* A,
+                  const void* B_t, const void* C_t, const float* D, const void* z_t,
+                  const float* delta_bias, int softplus, int64_t Bsz, int64_t Dch, int64_t N,
+                  ss_dtype dtype, void* y_t, ss_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SELSCAN_H_ */

@@ -1,0 +1,241 @@
+"""libselscan: the selective scan of the Mamba selective SSM on NVIDIA B300.
+
+Python binding of the C ABI in ``include/selscan.h``.  This module only
+marshals arguments (PyTorch supplies device memory and streams); every step
+of the computation runs in the CUDA kernels of ``libselscan.so``.  There is
+no CPU or PyTorch fallback: importing fails loudly when the library is
+missing or cannot be loaded.
+
+Entry points (same names as the C ABI):
+    ss_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
+                return_last_state=False) -> y | (y, h_last)
+    ss_scan_bwd(u, delta, A, B, C, D, z, delta_bias, softplus, dy) -> dict of grads
+    ss_step(h, u_t, delta_t, A, B_t, C_t, D=None, z_t=None, delta_bias=None,
+            softplus=True) -> y_t          (h updated in place)
+    ss_scan_bwd_workspace_size(Bsz, Dch, L, N, dtype) -> bytes
+and the autograd wrapper ``selective_scan`` (SelectiveScanFn).
+
+Layouts (channel-major, time innermost): u, delta, z, y: (Bsz, Dch, L);
+B, C: (Bsz, N, L); A: (Dch, N) float32; D, delta_bias: (Dch,) float32;
+h: (Bsz, Dch, N) float32.  A model holding activations as (B, L, D) (the
+"mamba.py" page's module boundary) transposes to (B, D, L) before the scan.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libselscan.so")
+
+SS_F32, SS_BF16 = 0, 1
+N_STATE = 16
+
+
+class SelscanError(RuntimeError):
+    """A libselscan call returned a non-zero ss_status."""
+
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {msg}")
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libselscan.so not found at {LIB_PATH}; build it with "
+            "`python selective_state_space_114_b300/build.py` (nvcc, sm_103a)")
+    lib = ctypes.CDLL(LIB_PATH)
+    p, i64, ci, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    lib.ss_status_str.argtypes = [ci]
+    lib.ss_status_str.restype = ctypes.c_char_p
+    lib.ss_version.argtypes = []
+    lib.ss_version.restype = ci
+    lib.ss_scan_fwd.argtypes = [p] * 8 + [ci, i64, i64, i64, i64, ci, p, p, p]
+    lib.ss_scan_fwd.restype = ci
+    lib.ss_scan_bwd_workspace_size.argtypes = [i64, i64, i64, i64, ci, ctypes.POINTER(sz)]
+    lib.ss_scan_bwd_workspace_size.restype = ci
+    lib.ss_scan_bwd.argtypes = ([p] * 8 + [ci, p, i64, i64, i64, i64, ci] + [p] * 8 +
+                                [p, sz, p])
+    lib.ss_scan_bwd.restype = ci
+    for name in ("ss_scan_bwd_states", "ss_scan_bwd_reverse", "ss_scan_bwd_reduce"):
+        f = getattr(lib, name)
+        f.argtypes = lib.ss_scan_bwd.argtypes
+        f.restype = ci
+    lib.ss_step.argtypes = [p] * 9 + [ci, i64, i64, i64, ci, p, p]
+    lib.ss_step.restype = ci
+    return lib
+
+
+_lib = _load()
+EXPORTED_SYMBOLS = ("ss_status_str", "ss_version", "ss_scan_fwd", "ss_scan_bwd_workspace_size",
+                    "ss_scan_bwd", "ss_scan_bwd_states", "ss_scan_bwd_reverse",
+                    "ss_scan_bwd_reduce", "ss_step")
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def ss_status_str(status: int) -> str:
+    return _lib.ss_status_str(int(status)).decode()
+
+
+def ss_version() -> int:
+    return int(_lib.ss_version())
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise SelscanError(fn, status, ss_status_str(status))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SS_F32
+    if t.dtype == torch.bfloat16:
+        return SS_BF16
+    raise TypeError(f"I/O dtype must be float32 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libselscan takes CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("libselscan takes contiguous tensors")
+    return t.data_ptr()
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _same(t, shape, dtype, name):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+
+
+def _check_scan_inputs(u, delta, A, B, C, D, z, delta_bias):
+    Bsz, Dch, L = u.shape
+    N = A.shape[1]
+    io = u.dtype
+    _same(delta, (Bsz, Dch, L), io, "delta")
+    if z is not None:
+        _same(z, (Bsz, Dch, L), io, "z")
+    _same(B, (Bsz, N, L), io, "B")
+    _same(C, (Bsz, N, L), io, "C")
+    _same(A, (Dch, N), torch.float32, "A")
+    if D is not None:
+        _same(D, (Dch,), torch.float32, "D")
+    if delta_bias is not None:
+        _same(delta_bias, (Dch,), torch.float32, "delta_bias")
+    return Bsz, Dch, L, N
+
+
+def ss_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
+                return_last_state=False, out=None, h_last=None):
+    """Forward selective scan on the current CUDA stream; returns y (and the
+    final state when return_last_state)."""
+    Bsz, Dch, L, N = _check_scan_inputs(u, delta, A, B, C, D, z, delta_bias)
+    y = torch.empty_like(u) if out is None else out
+    if return_last_state and h_last is None:
+        h_last = torch.empty((Bsz, Dch, N), device=u.device, dtype=torch.float32)
+    st = _lib.ss_scan_fwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                          _ptr(delta_bias), int(bool(softplus)), Bsz, Dch, L, N, _dtype_code(u),
+                          _ptr(y), _ptr(h_last), _stream(u.device))
+    _check("ss_scan_fwd", st)
+    return (y, h_last) if return_last_state else y
+
+
+def ss_scan_bwd_workspace_size(Bsz, Dch, L, N=N_STATE, dtype=SS_F32) -> int:
+    n = ctypes.c_size_t(0)
+    _check("ss_scan_bwd_workspace_size",
+           _lib.ss_scan_bwd_workspace_size(Bsz, Dch, L, N, dtype, ctypes.byref(n)))
+    return int(n.value)
+
+
+def ss_scan_bwd(u, delta, A, B, C, D, z, delta_bias, softplus, dy, workspace=None, out=None,
+                stages=("ss_scan_bwd",)):
+    """Backward of ss_scan_fwd.  Returns dict du, ddelta, dA, dB, dC, dD, dz,
+    ddelta_bias (None for absent optional inputs).  ``workspace``: optional
+    uint8 CUDA tensor of at least ss_scan_bwd_workspace_size bytes.
+    ``stages``: the C entry points to call in order (default the whole
+    backward; ("ss_scan_bwd_states", "ss_scan_bwd_reverse", "ss_scan_bwd_reduce")
+    is equivalent, one stage per call)."""
+    Bsz, Dch, L, N = _check_scan_inputs(u, delta, A, B, C, D, z, delta_bias)
+    _same(dy, (Bsz, Dch, L), u.dtype, "dy")
+    dev = u.device
+    f32 = torch.float32
+    g = out if out is not None else {
+        "du": torch.empty_like(u), "ddelta": torch.empty_like(u),
+        "dA": torch.empty((Dch, N), device=dev, dtype=f32),
+        "dB": torch.empty((Bsz, N, L), device=dev, dtype=f32),
+        "dC": torch.empty((Bsz, N, L), device=dev, dtype=f32),
+        "dD": torch.empty((Dch,), device=dev, dtype=f32) if D is not None else None,
+        "dz": torch.empty_like(u) if z is not None else None,
+        "ddelta_bias": torch.empty((Dch,), device=dev, dtype=f32) if delta_bias is not None else None,
+    }
+    need = ss_scan_bwd_workspace_size(Bsz, Dch, L, N, _dtype_code(u))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), device=dev, dtype=torch.uint8)
+    args = (_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+            int(bool(softplus)), _ptr(dy), Bsz, Dch, L, N, _dtype_code(u), _ptr(g["du"]),
+            _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]),
+            _ptr(g["dz"]), _ptr(g["ddelta_bias"]), _ptr(workspace), workspace.numel(),
+            _stream(dev))
+    for name in stages:
+        if name not in ("ss_scan_bwd", "ss_scan_bwd_states", "ss_scan_bwd_reverse",
+                        "ss_scan_bwd_reduce"):
+            raise ValueError(name)
+        _check(name, getattr(_lib, name)(*args))
+    return g
+
+
+def ss_step(h, u_t, delta_t, A, B_t, C_t, D=None, z_t=None, delta_bias=None, softplus=True,
+            out=None):
+    """One decode step; h (Bsz, Dch, N) float32 is updated in place.  Returns y_t."""
+    Bsz, Dch, N = h.shape
+    _same(h, (Bsz, Dch, N), torch.float32, "h")
+    io = u_t.dtype
+    _same(u_t, (Bsz, Dch), io, "u_t")
+    _same(delta_t, (Bsz, Dch), io, "delta_t")
+    if z_t is not None:
+        _same(z_t, (Bsz, Dch), io, "z_t")
+    _same(B_t, (Bsz, N), io, "B_t")
+    _same(C_t, (Bsz, N), io, "C_t")
+    _same(A, (Dch, N), torch.float32, "A")
+    y = torch.empty_like(u_t) if out is None else out
+    st = _lib.ss_step(_ptr(h), _ptr(u_t), _ptr(delta_t), _ptr(A), _ptr(B_t), _ptr(C_t), _ptr(D),
+                      _ptr(z_t), _ptr(delta_bias), int(bool(softplus)), Bsz, Dch, N,
+                      _dtype_code(u_t), _ptr(y), _stream(h.device))
+    _check("ss_step", st)
+    return y
+
+
+class SelectiveScanFn(torch.autograd.Function):
+    """Autograd wrapper: forward = ss_scan_fwd, backward = ss_scan_bwd
+    (recomputes the states; saves only the inputs)."""
+
+    @staticmethod
+    def forward(ctx, u, delta, A, B, C, D, z, delta_bias, softplus):
+        ctx.softplus = bool(softplus)
+        ctx.save_for_backward(u, delta, A, B, C, D, z, delta_bias)
+        return ss_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus)
+
+    @staticmethod
+    def backward(ctx, dy):
+        u, delta, A, B, C, D, z, delta_bias = ctx.saved_tensors
+        g = ss_scan_bwd(u, delta, A, B, C, D, z, delta_bias, ctx.softplus, dy.contiguous())
+        return (g["du"], g["ddelta"], g["dA"], g["dB"].to(B.dtype), g["dC"].to(C.dtype),
+                g["dD"], g["dz"], g["ddelta_bias"], None)
+
+
+def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True):
+    """Differentiable selective scan (see SelectiveScanFn)."""
+    return SelectiveScanFn.apply(u, delta, A, B, C, D, z, delta_bias, softplus)

@@ -1,0 +1,198 @@
+// C ABI of libselscan: argument checks, then dispatch to the kernels on the
+// caller's stream.  Declarations and contracts: include/selscan.h.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/selscan.h"
+#include "launch.h"
+
+using selscan::Dt;
+
+namespace {
+
+constexpr int64_t kMaxDim = int64_t(1) << 40;
+
+bool misaligned(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u); }
+
+bool bad_size(int64_t x) { return x < 0 || x > kMaxDim; }
+
+bool product_too_big(int64_t a, int64_t b, int64_t c) {
+  // a*b*c*16 (state-expanded element count) must fit comfortably in int64
+  if (a == 0 || b == 0 || c == 0) return false;
+  const double p = (double)a * (double)b * (double)c;
+  return p > 1e17;
+}
+
+ss_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SS_OK : SS_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* ss_status_str(ss_status s) {
+  switch (s) {
+    case SS_OK: return "SS_OK";
+    case SS_ERR_NULL: return "SS_ERR_NULL: a required pointer is NULL";
+    case SS_ERR_SHAPE: return "SS_ERR_SHAPE: a size is negative or too large";
+    case SS_ERR_DTYPE: return "SS_ERR_DTYPE: unknown dtype";
+    case SS_ERR_N_UNSUPPORTED: return "SS_ERR_N_UNSUPPORTED: N must be 16";
+    case SS_ERR_ALIGN: return "SS_ERR_ALIGN: a pointer is not 16-byte aligned";
+    case SS_ERR_WORKSPACE: return "SS_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case SS_ERR_CUDA: return "SS_ERR_CUDA: the CUDA runtime reported an error";
+  }
+  return "unknown ss_status";
+}
+
+int ss_version(void) { return 10000; }
+
+ss_status ss_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
+                      const void* C, const float* D, const void* z, const float* delta_bias,
+                      int softplus, int64_t Bsz, int64_t Dch, int64_t L, int64_t N,
+                      ss_dtype dtype, void* y, float* h_last, ss_stream_t stream) {
+  if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_DTYPE;
+  if (bad_size(Bsz) || bad_size(Dch) || bad_size(L) || bad_size(N)) return SS_ERR_SHAPE;
+  if (Bsz > 65535 || product_too_big(Bsz, Dch, L)) return SS_ERR_SHAPE;
+  if (N != 16) return SS_ERR_N_UNSUPPORTED;
+  const bool work = Bsz > 0 && Dch > 0 && L > 0;
+  if (work && (!u || !delta || !A || !B || !C || !y)) return SS_ERR_NULL;
+  if (misaligned(u) || misaligned(delta) || misaligned(A) || misaligned(B) || misaligned(C) ||
+      misaligned(D) || misaligned(z) || misaligned(delta_bias) || misaligned(y) ||
+      misaligned(h_last))
+    return SS_ERR_ALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!work) {
+    if (h_last && Bsz > 0 && Dch > 0)
+      return cuda_status(cudaMemsetAsync(h_last, 0, sizeof(float) * (size_t)(Bsz * Dch * N), s));
+    return SS_OK;
+  }
+  selscan::ScanArgs a{u, delta, A, B, C, D, z, delta_bias, softplus ? 1 : 0,
+                      Bsz, Dch, L, dtype == SS_BF16 ? Dt::BF16 : Dt::F32};
+  return cuda_status(selscan::launch_scan_fwd(a, y, h_last, s));
+}
+
+ss_status ss_scan_bwd_workspace_size(int64_t Bsz, int64_t Dch, int64_t L, int64_t N,
+                                     ss_dtype dtype, size_t* bytes) {
+  if (!bytes) return SS_ERR_NULL;
+  if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_DTYPE;
+  if (bad_size(Bsz) || bad_size(Dch) || bad_size(L) || bad_size(N)) return SS_ERR_SHAPE;
+  if (Bsz > 65535 || product_too_big(Bsz, Dch, L)) return SS_ERR_SHAPE;
+  if (N != 16) return SS_ERR_N_UNSUPPORTED;
+  *bytes = (Bsz > 0 && Dch > 0 && L > 0) ? selscan::bwd_workspace_bytes(Bsz, Dch, L) : 0;
+  return SS_OK;
+}
+
+namespace {
+
+// Checks shared by ss_scan_bwd and its three stages.  Returns SS_OK with
+// *work = false when there is nothing to compute (the zero gradients have
+// then been written by zero_grads when phase covers them).
+ss_status check_bwd(const void* u, const void* delta, const float* A, const void* B,
+                    const void* C, const float* D, const void* z, const float* delta_bias,
+                    const void* dy, int64_t Bsz, int64_t Dch, int64_t L, int64_t N,
+                    ss_dtype dtype, void* du, void* ddelta, float* dA, float* dB, float* dC,
+                    float* dD, void* dz, float* ddelta_bias, void* workspace,
+                    size_t workspace_bytes, bool* work) {
+  if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_DTYPE;
+  if (bad_size(Bsz) || bad_size(Dch) || bad_size(L) || bad_size(N)) return SS_ERR_SHAPE;
+  if (Bsz > 65535 || product_too_big(Bsz, Dch, L)) return SS_ERR_SHAPE;
+  if (N != 16) return SS_ERR_N_UNSUPPORTED;
+  *work = Bsz > 0 && Dch > 0 && L > 0;
+  if (*work && (!u || !delta || !A || !B || !C || !dy || !du || !ddelta || !dA || !dB || !dC))
+    return SS_ERR_NULL;
+  if (*work && ((D != nullptr) != (dD != nullptr) || (z != nullptr) != (dz != nullptr) ||
+                (delta_bias != nullptr) != (ddelta_bias != nullptr)))
+    return SS_ERR_NULL;
+  if (misaligned(u) || misaligned(delta) || misaligned(A) || misaligned(B) || misaligned(C) ||
+      misaligned(D) || misaligned(z) || misaligned(delta_bias) || misaligned(dy) ||
+      misaligned(du) || misaligned(ddelta) || misaligned(dA) || misaligned(dB) ||
+      misaligned(dC) || misaligned(dD) || misaligned(dz) || misaligned(ddelta_bias))
+    return SS_ERR_ALIGN;
+  if (*work) {
+    const size_t need = selscan::bwd_workspace_bytes(Bsz, Dch, L);
+    if (!workspace || misaligned(workspace) || workspace_bytes < need) return SS_ERR_WORKSPACE;
+  }
+  return SS_OK;
+}
+
+// Empty sequence or batch: every gradient that has elements is zero.
+ss_status zero_grads(int64_t Bsz, int64_t Dch, int64_t L, int64_t N, float* dA, float* dB,
+                     float* dC, float* dD, float* ddelta_bias, cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
+  if (Dch > 0) {
+    if (dA) e = cudaMemsetAsync(dA, 0, sizeof(float) * (size_t)(Dch * N), s);
+    if (e == cudaSuccess && dD) e = cudaMemsetAsync(dD, 0, sizeof(float) * (size_t)Dch, s);
+    if (e == cudaSuccess && ddelta_bias)
+      e = cudaMemsetAsync(ddelta_bias, 0, sizeof(float) * (size_t)Dch, s);
+  }
+  if (e == cudaSuccess && Bsz > 0 && L > 0) {
+    if (dB) e = cudaMemsetAsync(dB, 0, sizeof(float) * (size_t)(Bsz * N * L), s);
+    if (e == cudaSuccess && dC) e = cudaMemsetAsync(dC, 0, sizeof(float) * (size_t)(Bsz * N * L), s);
+  }
+  return cuda_status(e);
+}
+
+// phase < 0: all three stages in order; 0, 1, 2: one stage.
+ss_status run_bwd(int phase, const void* u, const void* delta, const float* A, const void* B,
+                  const void* C, const float* D, const void* z, const float* delta_bias,
+                  int softplus, const void* dy, int64_t Bsz, int64_t Dch, int64_t L, int64_t N,
+                  ss_dtype dtype, void* du, void* ddelta, float* dA, float* dB, float* dC,
+                  float* dD, void* dz, float* ddelta_bias, void* workspace,
+                  size_t workspace_bytes, ss_stream_t stream) {
+  bool work = false;
+  ss_status st = check_bwd(u, delta, A, B, C, D, z, delta_bias, dy, Bsz, Dch, L, N, dtype, du,
+                           ddelta, dA, dB, dC, dD, dz, ddelta_bias, workspace, workspace_bytes,
+                           &work);
+  if (st != SS_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!work) {
+    if (phase < 0 || phase == 2) return zero_grads(Bsz, Dch, L, N, dA, dB, dC, dD, ddelta_bias, s);
+    return SS_OK;
+  }
+  selscan::ScanArgs a{u, delta, A, B, C, D, z, delta_bias, softplus ? 1 : 0,
+                      Bsz, Dch, L, dtype == SS_BF16 ? Dt::BF16 : Dt::F32};
+  selscan::BwdOut o{dy, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias};
+  for (int ph = 0; ph < 3; ++ph) {
+    if (phase >= 0 && ph != phase) continue;
+    cudaError_t e = selscan::launch_scan_bwd(ph, a, o, workspace, s);
+    if (e != cudaSuccess) return SS_ERR_CUDA;
+  }
+  return SS_OK;
+}
+
+}  // namespace
+
+#define SS_BWD_PARAMS                                                                        \
+  const void *u, const void *delta, const float *A, const void *B, const void *C,             \
+      const float *D, const void *z, const float *delta_bias, int softplus, const void *dy,    \
+      int64_t Bsz, int64_t Dch, int64_t L, int64_t N, ss_dtype dtype, void *du, void *ddelta, \
+      float *dA, float *dB, float *dC, float *dD, void *dz, float *ddelta_bias,               \
+      void *workspace, size_t workspace_bytes, ss_stream_t stream
+#define SS_BWD_ARGS                                                                          \
+  u, delta, A, B, C, D, z, delta_bias, softplus, dy, Bsz, Dch, L, N, dtype, du, ddelta, dA, dB, \
+      dC, dD, dz, ddelta_bias, workspace, workspace_bytes, stream
+
+ss_status ss_scan_bwd(SS_BWD_PARAMS) { return run_bwd(-1, SS_BWD_ARGS); }
+ss_status ss_scan_bwd_states(SS_BWD_PARAMS) { return run_bwd(0, SS_BWD_ARGS); }
+ss_status ss_scan_bwd_reverse(SS_BWD_PARAMS) { return run_bwd(1, SS_BWD_ARGS); }
+ss_status ss_scan_bwd_reduce(SS_BWD_PARAMS) { return run_bwd(2, SS_BWD_ARGS); }
+
+ss_status ss_step(float* h, const void* u_t, const void* delta_t, const float* A,
+                  const void* B_t, const void* C_t, const float* D, const void* z_t,
+                  const float* delta_bias, int softplus, int64_t Bsz, int64_t Dch, int64_t N,
+                  ss_dtype dtype, void* y_t, ss_stream_t stream) {
+  if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_DTYPE;
+  if (bad_size(Bsz) || bad_size(Dch) || bad_size(N)) return SS_ERR_SHAPE;
+  if (product_too_big(Bsz, Dch, 4)) return SS_ERR_SHAPE;
+  if (N != 16) return SS_ERR_N_UNSUPPORTED;
+  if (Bsz == 0 || Dch == 0) return SS_OK;
+  if (!h || !u_t || !delta_t || !A || !B_t || !C_t || !y_t) return SS_ERR_NULL;
+  if (misaligned(h) || misaligned(u_t) || misaligned(delta_t) || misaligned(A) ||
+      misaligned(B_t) || misaligned(C_t) || misaligned(D) || misaligned(z_t) ||
+      misaligned(delta_bias) || misaligned(y_t))
+    return SS_ERR_ALIGN;
+  selscan::StepArgs a{h, u_t, delta_t, A, B_t, C_t, D, z_t, delta_bias, softplus ? 1 : 0,
+                      Bsz, Dch, dtype == SS_BF16 ? Dt::BF16 : Dt::F32, y_t};
+  return cuda_status(selscan::launch_step(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

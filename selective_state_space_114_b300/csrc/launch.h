@@ -1,0 +1,67 @@
+// Internal launcher interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace selscan {
+
+enum class Dt { F32 = 0, BF16 = 1 };
+
+struct ScanArgs {
+  const void* u;
+  const void* delta;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;           // nullable
+  const void* z;            // nullable
+  const float* delta_bias;  // nullable
+  int softplus;
+  int64_t Bsz, Dch, L;
+  Dt dt;
+};
+
+struct BwdOut {
+  const void* dy;
+  void* du;
+  void* ddelta;
+  float* dA;
+  float* dB;
+  float* dC;
+  float* dD;           // nullable iff D null
+  void* dz;            // nullable iff z null
+  float* ddelta_bias;  // nullable iff delta_bias null
+};
+
+struct StepArgs {
+  float* h;
+  const void* u;
+  const void* delta;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  const void* z;
+  const float* delta_bias;
+  int softplus;
+  int64_t Bsz, Dch;
+  Dt dt;
+  void* y;
+};
+
+// Forward: writes y and (if non-null) h_last.  Requires Bsz*Dch*L > 0.
+cudaError_t launch_scan_fwd(const ScanArgs& a, void* y, float* h_last, cudaStream_t s);
+
+// Backward workspace size (bytes) and the launch of one of its three stages
+// (phase 0: segment states, 1: reverse pass, 2: reduction of the partials).
+// Requires Bsz*Dch*L > 0.
+size_t bwd_workspace_bytes(int64_t Bsz, int64_t Dch, int64_t L);
+cudaError_t launch_scan_bwd(int phase, const ScanArgs& a, const BwdOut& o, void* ws,
+                            cudaStream_t s);
+
+// One decode step.  Requires Bsz*Dch > 0.
+cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
+
+}  // namespace selscan

@@ -1,0 +1,153 @@
+"""Forward scan on the GPU (through the C ABI binding) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity_util import (check, inputs_to_dev, make_case, oracle_fwd, out_kind, to_host64,
+                         widen_all)
+
+import selective_state_space_114_b300 as ss
+
+pytestmark = pytest.mark.gpu
+
+
+def run_fwd(xd, softplus=True, last=True):
+    return ss.ss_scan_fwd(xd["u"], xd["delta"], xd["A"], xd["B"], xd["C"], xd.get("D"),
+                          xd.get("z"), xd.get("delta_bias"), softplus, return_last_state=last)
+
+
+def compare(x, dtype, softplus=True, what=""):
+    xd = inputs_to_dev(x, dtype)
+    y, hl = run_fwd(xd, softplus)
+    torch.cuda.synchronize()
+    ref, href = oracle_fwd(x, softplus)
+    check(to_host64(y), ref, out_kind(dtype), f"{what} y")
+    check(to_host64(hl), href, "f32" if dtype == "f32" else "bf16", f"{what} h_last")
+
+
+def test_tiny_config_f32():
+    cfg = synth.config(0)
+    compare(synth.make_inputs(cfg), "f32", what="tiny")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("Bsz,Dch,L", [
+    (3, 20, 1000),   # several chunks + ragged tail, channels not a multiple of the CTA
+    (1, 16, 256),    # exactly one chunk
+    (2, 17, 257),    # one step past a chunk
+    (2, 5, 16),      # one lane segment
+    (1, 3, 1),       # a single step
+    (2, 9, 37),      # L not a multiple of the vector width (element-wise path)
+    (1, 33, 2050),   # ragged at the vector width for f32 only
+])
+def test_shapes(dtype, Bsz, Dch, L):
+    x = make_case(dtype, Bsz, Dch, L, seed=100 + L + Dch)
+    compare(x, dtype, what=f"{dtype} {Bsz}x{Dch}x{L}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("drop", ["D", "z", "delta_bias", "all", "softplus"])
+def test_optional_inputs(dtype, drop):
+    x = make_case(dtype, 2, 18, 700, seed=7)
+    softplus = True
+    if drop == "all":
+        x.update(D=None, z=None, delta_bias=None)
+    elif drop == "softplus":
+        softplus = False
+        # raw deltas must be positive-ish for a decaying state: use |delta| * 0.05
+        d = synth.widen(x["delta"])
+        d = np.abs(d) * 0.05
+        x["delta"] = synth.to_bf16(d.astype(np.float32)) if dtype == "bf16" else d.astype(np.float32)
+        x["delta_bias"] = np.zeros_like(x["delta_bias"])
+    else:
+        x[drop] = None
+    compare(x, dtype, softplus=softplus, what=f"{dtype} drop={drop}")
+
+
+def test_empty_inputs():
+    dev = "cuda"
+    A = torch.full((4, 16), -1.0, device=dev)
+    for Bsz, Dch, L in [(2, 4, 0), (0, 4, 8)]:
+        u = torch.zeros((Bsz, Dch, L), device=dev)
+        B = torch.zeros((Bsz, 16, L), device=dev)
+        y, hl = ss.ss_scan_fwd(u, u, A[:Dch].contiguous(), B, B, return_last_state=True)
+        torch.cuda.synchronize()
+        assert y.shape == (Bsz, Dch, L)
+        assert hl.shape == (Bsz, Dch, 16) and torch.all(hl == 0)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_no_writes_outside_outputs(dtype):
+    """Guard regions around y and h_last must be untouched (bounds of every store)."""
+    x = make_case(dtype, 2, 19, 300, seed=9)
+    xd = inputs_to_dev(x, dtype)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    pad = 64
+    n = 2 * 19 * 300
+    ybuf = torch.full((n + 2 * pad,), 7.0, device="cuda", dtype=tdt)
+    hbuf = torch.full((2 * 19 * 16 + 2 * pad,), 7.0, device="cuda", dtype=torch.float32)
+    y = ybuf[pad : pad + n].view(2, 19, 300)
+    hl = hbuf[pad : pad + 2 * 19 * 16].view(2, 19, 16)
+    ss.ss_scan_fwd(xd["u"], xd["delta"], xd["A"], xd["B"], xd["C"], xd["D"], xd["z"],
+                   xd["delta_bias"], True, out=y, h_last=hl, return_last_state=True)
+    torch.cuda.synchronize()
+    assert torch.all(ybuf[:pad] == 7.0) and torch.all(ybuf[pad + n :] == 7.0)
+    assert torch.all(hbuf[:pad] == 7.0) and torch.all(hbuf[pad + 2 * 19 * 16 :] == 7.0)
+    ref, _ = oracle_fwd(x)
+    check(to_host64(y), ref, out_kind(dtype), "guarded y")
+
+
+def test_deterministic():
+    x = make_case("bf16", 2, 40, 1500, seed=11)
+    xd = inputs_to_dev(x, "bf16")
+    y1, h1 = run_fwd(xd)
+    y2, h2 = run_fwd(xd)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2) and torch.equal(h1, h2)
+
+
+def _row_oracle(cfg, b, d):
+    r = synth.row_inputs(cfg, b, d)
+    w = widen_all(r)
+    L, N = cfg["L"], cfg["N"]
+    out, hl = oracle.scan_fwd(w["u"].reshape(1, 1, L), w["delta"].reshape(1, 1, L),
+                              w["A"].reshape(1, N), w["B"].reshape(1, N, L),
+                              w["C"].reshape(1, N, L), w["D"], w["z"].reshape(1, 1, L),
+                              w["delta_bias"], True)
+    return out[0, 0], hl[0, 0]
+
+
+def _full_config_sampled(index, rows):
+    cfg = synth.config(index)
+    x = synth.make_inputs(cfg)
+    xd = inputs_to_dev(x, cfg["dtype"])
+    del x
+    y, hl = run_fwd(xd)
+    torch.cuda.synchronize()
+    assert torch.isfinite(y.float()).all()
+    L = cfg["L"]
+    for b, d in rows:
+        ref, href = _row_oracle(cfg, b, d)
+        got = to_host64(y[b, d])
+        check(got, ref, out_kind(cfg["dtype"]), f"config {index} row ({b},{d})")
+        check(to_host64(hl[b, d]), href, "bf16", f"config {index} h_last ({b},{d})")
+        # error per chunk of L, relative to the bound, must not grow along the sequence
+        if L >= 8192:
+            err = np.abs(got - ref) / (2e-2 * (np.abs(ref) + 1e-2))
+            per = err[: (L // 4096) * 4096].reshape(-1, 4096).max(axis=1)
+            assert per.max() <= 1.0
+
+
+def test_config1_full_size_sampled_rows():
+    rng = np.random.default_rng(1)
+    rows = [(0, 0), (7, 1535), (3, 767)] + [(int(rng.integers(8)), int(rng.integers(1536)))
+                                            for _ in range(29)]
+    _full_config_sampled(1, rows)
+
+
+def test_config3_full_size_sampled_rows():
+    rng = np.random.default_rng(3)
+    rows = [(0, 0), (0, 5119)] + [(0, int(rng.integers(5120))) for _ in range(6)]
+    _full_config_sampled(3, rows)
