@@ -67,7 +67,9 @@ typedef enum {
     SS_ERR_N_UNSUPPORTED = 4,  /* N != 16                                         */
     SS_ERR_ALIGN = 5,          /* a pointer is not 16-byte aligned                */
     SS_ERR_WORKSPACE = 6,      /* workspace NULL/misaligned or smaller than needed */
-    SS_ERR_CUDA = 7            /* the CUDA runtime reported a launch error        */
+    SS_ERR_CUDA = 7,           /* the CUDA runtime reported a launch error        */
+    SS_ERR_SCRATCH_LIMIT = 8   /* ss_scan_bwd_noalloc: problem needs more scratch
+                                  than the library's static buffer holds          */
 } ss_status;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -167,6 +169,42 @@ ss_status ss_step(float* h, const void* u_t, const void* delta_t, const float* A
                   const void* B_t, const void* C_t, const float* D, const void* z_t,
                   const float* delta_bias, int softplus, int64_t Bsz, int64_t Dch, int64_t N,
                   ss_dtype dtype, void* y_t, ss_stream_t stream);
+
+/*
+ * Backward scan for callers that cannot allocate device memory.
+ *
+ * The pages describe no counterpart of this entry point; it exists for
+ * library users only.  Some callers cannot call cudaMalloc: a plugin running
+ * inside a host application that owns every device allocation, or a
+ * latency-critical loop that must never enter the allocator (which can
+ * synchronise the device).  They can pass inputs and outputs but no
+ * workspace.  This call is ss_scan_bwd with the workspace taken from a
+ * scratch buffer compiled into the library: a static device array of
+ * ss_scan_bwd_noalloc_max_scratch() bytes (32 MiB), which every GPU that
+ * loads the library holds until the process exits.
+ *   - Arguments, checks, outputs and results are those of ss_scan_bwd,
+ *     without the workspace pair.
+ *   - Sizes whose ss_scan_bwd_workspace_size exceeds the buffer are
+ *     rejected with SS_ERR_SCRATCH_LIMIT; nothing is launched.
+ *   - The first call on a device looks up the buffer's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture starts.
+ *   - The call allocates nothing (no cudaMalloc, cudaFree or allocating
+ *     library routine).
+ *   - All calls share the one buffer, which keeps the last call's contents;
+ *     the kernels write every scratch word before reading it, so nothing is
+ *     cleared.  Calls that overlap on the GPU (e.g. unordered streams) race
+ *     on the buffer: order them.
+ */
+ss_status ss_scan_bwd_noalloc(const void* u, const void* delta, const float* A, const void* B,
+                              const void* C, const float* D, const void* z,
+                              const float* delta_bias, int softplus, const void* dy,
+                              int64_t Bsz, int64_t Dch, int64_t L, int64_t N, ss_dtype dtype,
+                              void* du, void* ddelta, float* dA, float* dB, float* dC,
+                              float* dD, void* dz, float* ddelta_bias, ss_stream_t stream);
+
+/* Size in bytes of the static scratch buffer ss_scan_bwd_noalloc uses. */
+size_t ss_scan_bwd_noalloc_max_scratch(void);
 
 #ifdef __cplusplus
 }

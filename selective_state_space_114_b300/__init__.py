@@ -66,13 +66,18 @@ def _load() -> ctypes.CDLL:
         f.restype = ci
     lib.ss_step.argtypes = [p] * 9 + [ci, i64, i64, i64, ci, p, p]
     lib.ss_step.restype = ci
+    lib.ss_scan_bwd_noalloc.argtypes = [p] * 8 + [ci, p, i64, i64, i64, i64, ci] + [p] * 9
+    lib.ss_scan_bwd_noalloc.restype = ci
+    lib.ss_scan_bwd_noalloc_max_scratch.argtypes = []
+    lib.ss_scan_bwd_noalloc_max_scratch.restype = sz
     return lib
 
 
 _lib = _load()
 EXPORTED_SYMBOLS = ("ss_status_str", "ss_version", "ss_scan_fwd", "ss_scan_bwd_workspace_size",
                     "ss_scan_bwd", "ss_scan_bwd_states", "ss_scan_bwd_reverse",
-                    "ss_scan_bwd_reduce", "ss_step")
+                    "ss_scan_bwd_reduce", "ss_step", "ss_scan_bwd_noalloc",
+                    "ss_scan_bwd_noalloc_max_scratch")
 
 
 def lib() -> ctypes.CDLL:

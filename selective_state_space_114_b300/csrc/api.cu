@@ -39,6 +39,9 @@ const char* ss_status_str(ss_status s) {
     case SS_ERR_ALIGN: return "SS_ERR_ALIGN: a pointer is not 16-byte aligned";
     case SS_ERR_WORKSPACE: return "SS_ERR_WORKSPACE: workspace missing, misaligned or too small";
     case SS_ERR_CUDA: return "SS_ERR_CUDA: the CUDA runtime reported an error";
+    case SS_ERR_SCRATCH_LIMIT:
+      return "SS_ERR_SCRATCH_LIMIT: the problem needs more scratch than the static buffer of "
+             "ss_scan_bwd_noalloc holds";
   }
   return "unknown ss_status";
 }
