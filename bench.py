@@ -42,12 +42,17 @@ UNIT = "Gelem/s"
 CFG_INDEX = 1
 N_STATE = 16
 
-# Hardware figures for the roofline denominators.
+# Hardware figures for the roofline denominators (one B300).
 SMS = 148
 SM_MAX_MHZ = 2032.0
-FP32_LANES = 128            # FP32 ops per clock per SM (one per lane)
-ALU_PEAK_TOPS = SMS * FP32_LANES * SM_MAX_MHZ * 1e6 / 1e12   # 38.49 T ops/s
+FP32_LANES = 128            # FP32 operations per clock per SM
+MUFU_LANES = 32             # MUFU (ex2 / lg2 / rcp) results per clock per SM, measured
+FP32_PEAK_T = SMS * FP32_LANES * SM_MAX_MHZ * 1e6 / 1e12   # 38.49 T ops/s
+MUFU_PEAK_T = SMS * MUFU_LANES * SM_MAX_MHZ * 1e6 / 1e12   # 9.62 T ops/s
 L2_BYTES = 126 * 2 ** 20
+# kernels one step launches: forward 1; backward states 2 (chunk summaries,
+# chunk carries), reverse 1, reduce 2 (dB/dC, dA/dD/dbias); decode step 1
+LAUNCHES_PER_STEP = 7
 
 
 def load_peaks():
@@ -60,49 +65,59 @@ def load_peaks():
 
 
 # ---------------------------------------------------------------------------
-# Algorithmic work per scanned element (b, d, t) of each kernel, N = 16,
-# s = bytes per I/O element, Dch = channels.  "ops" counts FP32 and MUFU
-# operations (one issue slot each); bytes count each tensor read or written
-# once.
-#   fwd:         MUFU N+4 (N decays, softplus 2, sigmoid 2); FP32 4N+10
-#                (per state: delta*A, delta*u*B, state FMA, output FMA).
-#                bytes 4s + 2Ns/Dch (u, delta, z in; y out; B, C per (b,t)).
-#   bwd_states:  MUFU N+2; FP32 3N+5 (decay argument, input term, fold FMA).
-#                bytes 2s + 4 + Ns/Dch (u, delta in; one f32 state per
-#                16 steps and state out).
-#   bwd_reverse: MUFU N+6; FP32 14N+20 (decay arg, state replay 2, output
-#                for dz, adjoint 2, dC, dB, du-sum, ddelta-sum 2, dA, the
-#                two row sums of dB and dC).
-#                bytes 7s + 4 + 2Ns/Dch (u, delta, z, dy, states in;
-#                du, ddelta, dz out; B, C per (b,t)).
-#   bwd_reduce:  bytes 2N*4*(G+1)/Dch per element (G = Dch/16 partials of
-#                dB, dC read, dB, dC written); no arithmetic to speak of.
-#   step:        per (b,d) row: bytes 8N + 4s; MUFU N+4; FP32 4N+10.
+# Algorithmic work per scanned element (b, d, t) of each stage, N = 16,
+# s = bytes per I/O element, Dch = channels: what the method needs, not what
+# a kernel executes.  fp32 = FP32 add/mul/fma operations, mufu = exp / log /
+# reciprocal evaluations, bytes = each tensor read or written once.
+#   fwd:          per state: delta*A, delta*u*B, the state update, C*h (4N);
+#                 softplus 4, D skip 1, delta*u 1, gate 3; MUFU: N decays,
+#                 softplus 2, sigmoid 2.  Bytes: u, delta, z in, y out (4s)
+#                 plus B, C once per (b, t): 2Ns/Dch.
+#   bwd_states:   chunk summaries: per state delta*A, the input term, the
+#                 state fold, the decay product, yhat*C, the adjoint fold
+#                 (6N) + 12; MUFU N + 4.  Bytes: u, delta, z, dy in (4s) +
+#                 B, C + 33 floats out per 128 steps.
+#   bwd_reverse:  the backward proper: per state the recomputed decay and
+#                 state (3), adjoint (2), dC, dB, du-sum, ddelta-sum (2),
+#                 dA, pre-gate output (7) = 12N; + 20 per element; MUFU N + 6.
+#                 Bytes: u, delta, z, dy in, du, ddelta, dz out (7s), B, C,
+#                 dB, dC written once per (b, t): (2Ns + 8N)/Dch.
+#   bwd_reduce:   dB/dC partials of 128-row blocks read, dB, dC written:
+#                 2N*4*(ceil(Dch/128) + 1)/Dch.
 # ---------------------------------------------------------------------------
 def kernel_work(s, Dch, N=N_STATE):
-    G = (Dch + 15) // 16
+    G = (Dch + 127) // 128
     return {
-        "fwd": dict(ops=(N + 4) + (4 * N + 10), bytes=4 * s + 2 * N * s / Dch),
-        "bwd_states": dict(ops=(N + 2) + (3 * N + 5), bytes=2 * s + 4 + N * s / Dch),
-        "bwd_reverse": dict(ops=(N + 6) + (14 * N + 20), bytes=7 * s + 4 + 2 * N * s / Dch),
-        "bwd_reduce": dict(ops=0, bytes=2 * N * 4 * (G + 1) / Dch),
+        "fwd": dict(fp32=4 * N + 9, mufu=N + 4, bytes=4 * s + 2 * N * s / Dch),
+        "bwd_states": dict(fp32=6 * N + 12, mufu=N + 4,
+                           bytes=4 * s + 2 * N * s / Dch + 33 * 4 / 128),
+        "bwd_reverse": dict(fp32=12 * N + 20, mufu=N + 6,
+                            bytes=7 * s + (2 * N * s + 8 * N) / Dch),
+        "bwd_reduce": dict(fp32=0, mufu=0, bytes=2 * N * 4 * (G + 1) / Dch),
     }
 
 
 def roofline(name, work, elems, ms, hbm_gbs, traffic=None):
+    """Roofline of one kernel: the binding resource is the one whose
+    algorithmic work takes longest at its peak; achieved = that work / the
+    measured time."""
     t = ms * 1e-3
-    t_alu = work["ops"] * elems / (ALU_PEAK_TOPS * 1e12)
-    t_hbm = work["bytes"] * elems / (hbm_gbs * 1e9)
-    if t_alu >= t_hbm:
-        ach = work["ops"] * elems / t / 1e12
-        return {"kernel": name, "bound": "alu", "achieved": round(ach, 3),
-                "peak": round(ALU_PEAK_TOPS, 2), "unit": "TOP/s", "frac": round(ach / ALU_PEAK_TOPS, 4),
-                "traffic": traffic, "algorithmic_ops": work["ops"] * elems,
-                "algorithmic_bytes": work["bytes"] * elems}
-    ach = work["bytes"] * elems / t / 1e9
-    return {"kernel": name, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_gbs,
-            "unit": "GB/s", "frac": round(ach / hbm_gbs, 4), "traffic": traffic,
-            "algorithmic_ops": work["ops"] * elems, "algorithmic_bytes": work["bytes"] * elems}
+    times = {"hbm": work["bytes"] * elems / (hbm_gbs * 1e9),
+             "fp32": work["fp32"] * elems / (FP32_PEAK_T * 1e12),
+             "mufu": work["mufu"] * elems / (MUFU_PEAK_T * 1e12)}
+    res = max(times, key=times.get)
+    base = {"kernel": name, "traffic": traffic, "resource": res,
+            "algorithmic_bytes": work["bytes"] * elems, "algorithmic_fp32": work["fp32"] * elems,
+            "algorithmic_mufu": work["mufu"] * elems,
+            "bound_ms": {k: round(v * 1e3, 4) for k, v in times.items()}}
+    if res == "hbm":
+        ach = work["bytes"] * elems / t / 1e9
+        return {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_gbs, "unit": "GB/s",
+                "frac": round(ach / hbm_gbs, 4), **base}
+    peak = FP32_PEAK_T if res == "fp32" else MUFU_PEAK_T
+    ach = work[res] * elems / t / 1e12
+    return {"bound": "alu", "achieved": round(ach, 3), "peak": round(peak, 3), "unit": "TFLOP/s",
+            "frac": round(ach / peak, 4), **base}
 
 
 def csrc_digest():
@@ -130,75 +145,125 @@ def ncu_traffic(kernel):
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
+    """SM clock and clock-event reasons sampled while the timed region runs:
+    NVML when its library loads, else ``nvidia-smi --query-gpu ... -lms``."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
     def __init__(self, device_index=0):
-        self.samples = []
+        self.samples = []   # (sm_mhz, reasons bitmask or list of names)
         self._stop = threading.Event()
-        self.ok = False
+        self.mode = None
+        self.max_mhz = None
+        self.err = []
+        self.bus = None
+        try:
+            import torch
+            props = torch.cuda.get_device_properties(device_index)
+            self.bus = "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id,
+                                             props.pci_device_id)
+        except Exception as e:
+            self.err.append(f"pci id: {e}")
         try:
             import pynvml as nv
             nv.nvmlInit()
             self.nv = nv
-            handle = None
-            try:
-                import torch
-                props = torch.cuda.get_device_properties(device_index)
-                bus = "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id,
-                                            props.pci_device_id)
-                handle = nv.nvmlDeviceGetHandleByPciBusId(bus.encode())
-            except Exception:
-                handle = None
-            if handle is None:
-                handle = nv.nvmlDeviceGetHandleByIndex(device_index)
-            self.h = handle
-            self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(handle, nv.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception as e:  # no NVML: report what we could not sample
-            self.err = str(e)
+            self.h = (nv.nvmlDeviceGetHandleByPciBusId(self.bus.encode()) if self.bus
+                      else nv.nvmlDeviceGetHandleByIndex(device_index))
+            self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(self.h, nv.NVML_CLOCK_SM)
+            self.mode = "nvml"
+        except Exception as e:
+            self.err.append(f"nvml: {e}")
+            import shutil
+            if shutil.which("nvidia-smi"):
+                self.mode = "nvidia-smi"
 
-    def _reasons(self):
+    def _nvml_reasons(self):
         nv = self.nv
         try:
             return nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
         except Exception:
             return nv.nvmlDeviceGetCurrentClocksThrottleReasons(self.h)
 
-    def _run(self):
+    def _run_nvml(self):
         nv = self.nv
         while not self._stop.is_set():
             try:
                 self.samples.append((nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM),
-                                     int(self._reasons())))
+                                     int(self._nvml_reasons())))
             except Exception:
                 pass
             time.sleep(0.002)
 
+    def _start_smi(self):
+        import subprocess
+        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        cmd = ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "20"]
+        if self.bus:
+            cmd += ["-i", self.bus]
+        self._proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                      text=True)
+        time.sleep(0.3)  # let it take its first samples before the timed region
+
+    def _stop_smi(self):
+        self._proc.terminate()
+        out, _ = self._proc.communicate(timeout=10)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                mhz, mx = float(f[0]), float(f[1])
+                active = int(f[2], 16) if f[2].startswith("0x") else 0
+            except ValueError:
+                continue
+            self.max_mhz = mx
+            seen = [nm for nm, v in zip(names, f[3:7]) if v.lower() == "active"]
+            self.samples.append((mhz, active, seen))
+
     def __enter__(self):
-        if self.ok:
-            self._t = threading.Thread(target=self._run, daemon=True)
+        if self.mode == "nvml":
+            self._t = threading.Thread(target=self._run_nvml, daemon=True)
             self._t.start()
+        elif self.mode == "nvidia-smi":
+            try:
+                self._start_smi()
+            except Exception as e:
+                self.err.append(f"nvidia-smi: {e}")
+                self.mode = None
         return self
 
     def __exit__(self, *a):
-        if self.ok:
+        if self.mode == "nvml":
             self._stop.set()
             self._t.join()
+        elif self.mode == "nvidia-smi":
+            try:
+                self._stop_smi()
+            except Exception as e:
+                self.err.append(f"nvidia-smi: {e}")
 
     def summary(self):
-        if not self.ok:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
-        names = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
-                 0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
-                 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
-                 0x100: "display_clock_setting"}
+        if not self.mode:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clocks not sampled"],
+                    "errors": self.err}
         busy = [s for s in self.samples if not (s[1] & 0x1)] or self.samples
         seen = set()
-        for _, r in busy:
-            for bit, nm in names.items():
-                if r & bit:
+        for s in busy:
+            for bit, nm in self.REASONS.items():
+                if s[1] & bit:
                     seen.add(nm)
+            if len(s) > 2:
+                seen.update(s[2])
         mhz = statistics.median([s[0] for s in busy]) if busy else None
         return {"sm_mhz": mhz, "sm_max_mhz": self.max_mhz, "reasons": sorted(seen),
-                "samples": len(busy)}
+                "samples": len(busy), "source": self.mode}
 
 
 # ---------------------------------------------------------------------------
@@ -249,23 +314,35 @@ def oracle_sample_step(cfg, nch, seed):
 
 
 def size_oracle_sample(cfg, target_s, seed):
+    """Number of channels (all batches, full L) whose oracle pass takes about
+    target_s seconds on the host cores (capped at the whole workload)."""
     cores = os.cpu_count() or 1
-    n0 = max(2, min(cores, 8))
-    t = oracle_sample_step(cfg, n0, seed)
-    per_ch = t / n0
-    n = int(max(n0, min(cfg["Dch"], target_s / max(per_ch, 1e-9))))
+    n = max(2, min(cores, 8))
+    for _ in range(4):
+        t = oracle_sample_step(cfg, n, seed)
+        if t >= 0.5 * target_s or n >= cfg["Dch"]:
+            break
+        n = int(min(cfg["Dch"], max(2 * n, n * target_s / max(t, 1e-6))))
     return n
 
 
 def cpu_baseline(cfg, seed, target_s=12.0):
+    """The oracle as it stands, timed on the host cores: passes over the
+    first n channels (all batches, full L), repeated while the sample is
+    shorter than about target_s seconds."""
     import oracle
     cores = oracle.default_threads()
     n = size_oracle_sample(cfg, target_s, seed)
     t = oracle_sample_step(cfg, n, seed)
-    elems = cfg["Bsz"] * n * cfg["L"]
+    reps = 1
+    while t < 0.5 * target_s and reps < 64:
+        t += oracle_sample_step(cfg, n, seed)
+        reps += 1
+    elems = cfg["Bsz"] * n * cfg["L"] * reps
     return {"value": round(elems / t / 1e9, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"fp64 oracle fwd+bwd+1 step over all {cfg['Bsz']} batches x first {n} of "
-                      f"{cfg['Dch']} channels x L={cfg['L']} ({elems} elements, {t:.1f} s)"}
+            "sample": f"{reps} fp64 oracle pass(es) of fwd+bwd+1 step over all {cfg['Bsz']} "
+                      f"batches x first {n} of {cfg['Dch']} channels x L={cfg['L']} "
+                      f"({elems} elements, {t:.1f} s)"}
 
 
 def run_reference(args):
@@ -432,13 +509,14 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": conf,
         "fwd_gelem_s": round(fwd_gelem, 3),
         "roofline": roofs[dominant],
-        "roofline_peak_source": f"alu: {SMS} SMs x {FP32_LANES} FP32 ops/clk x {SM_MAX_MHZ} MHz; "
-                                f"hbm: {hbm} GB/s {peak_src}",
+        "roofline_peak_source": f"fp32: {SMS} SMs x {FP32_LANES} ops/clk x {SM_MAX_MHZ} MHz; "
+                                f"mufu: {SMS} SMs x {MUFU_LANES} ops/clk (measured) x "
+                                f"{SM_MAX_MHZ} MHz; hbm: {hbm} GB/s of {peak_src}",
         "kernels": {nm: {"ms": round(per_kernel[nm], 4),
                          "share": round(per_kernel[nm] / sum(per_kernel.values()), 4),
                          **({"frac": roofs[nm]["frac"], "bound": roofs[nm]["bound"]}
                             if nm in roofs else {})} for nm in names},
-        "gpu_launches": K * 6,
+        "gpu_launches": K * LAUNCHES_PER_STEP,
         "e2e": {"value": round(world * E / (e2e_ms * 1e-3) / 1e9, 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 3)},

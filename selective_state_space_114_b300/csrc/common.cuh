@@ -260,3 +260,299 @@ __device__ __forceinline__ void scan16_rev(float& P, float& S, int j) {
 }
 
 }  // namespace selscan
+
+// ===========================================================================
+// Building blocks of the paired-state kernels.
+//
+// Two states (n, n+1) travel together in a float2 and are updated by one
+// packed instruction (sm_100+ f32x2 arithmetic: two IEEE fp32 operations,
+// round-to-nearest, per instruction), which halves the issue slots of the
+// state recurrences.
+// ===========================================================================
+namespace selscan {
+
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+__device__ __forceinline__ float lg2f_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// softplus(x) = max(x, 0) + log1p(w), w = e^-|x| in (0, 1].
+// log1p(w): for w <= 1/32 the Mercator series w - w^2/2 + w^3/3 - w^4/4 + w^5/5
+// (truncation error below w^6/6, i.e. < 2e-10 relative); above, ln2 * log2(1 + w),
+// whose rounding of 1 + w costs at most ~2e-6 relative there.  One MUFU ex2 and
+// one MUFU lg2; accurate where the steps of a selective scan live (x << 0).
+__device__ __forceinline__ float softplus_fast(float x) {
+  const float w = ex2f(-fabsf(x) * kLog2e);
+  float s = fmaf(w, 0.2f, -0.25f);
+  s = fmaf(w, s, 0.33333334f);
+  s = fmaf(w, s, -0.5f);
+  s = fmaf(w, s, 1.f);
+  s *= w;
+  const float l = lg2f_approx(1.f + w) * 0.69314718f;
+  return fmaxf(x, 0.f) + (w <= 0.03125f ? s : l);
+}
+
+// Inclusive scan of the affine maps h -> P h + S on two states at once over
+// the RL segments of a row, earlier segments first.  The row's lanes are
+// lane0 + STRIDE * j, j = 0 .. RL-1 (STRIDE = 2: two rows interleaved in a
+// warp; STRIDE = 1 with RL-lane shuffle segments otherwise).
+template <int RL, int STRIDE>
+__device__ __forceinline__ void scan_pair_fwd(float2& P, float2& S, int j) {
+#pragma unroll
+  for (int off = 1; off < RL; off <<= 1) {
+    float2 Pp, Sp;
+    constexpr int Wd = STRIDE == 1 ? RL : 32;
+    Pp.x = __shfl_up_sync(0xffffffffu, P.x, STRIDE * off, Wd);
+    Pp.y = __shfl_up_sync(0xffffffffu, P.y, STRIDE * off, Wd);
+    Sp.x = __shfl_up_sync(0xffffffffu, S.x, STRIDE * off, Wd);
+    Sp.y = __shfl_up_sync(0xffffffffu, S.y, STRIDE * off, Wd);
+    if (j >= off) {
+      S = fma2(P, Sp, S);
+      P = mul2(P, Pp);
+    }
+  }
+}
+
+// Same with later segments applied first (the reverse-time adjoint recurrence).
+template <int RL, int STRIDE>
+__device__ __forceinline__ void scan_pair_rev(float2& P, float2& S, int j) {
+#pragma unroll
+  for (int off = 1; off < RL; off <<= 1) {
+    float2 Pn, Sn;
+    constexpr int Wd = STRIDE == 1 ? RL : 32;
+    Pn.x = __shfl_down_sync(0xffffffffu, P.x, STRIDE * off, Wd);
+    Pn.y = __shfl_down_sync(0xffffffffu, P.y, STRIDE * off, Wd);
+    Sn.x = __shfl_down_sync(0xffffffffu, S.x, STRIDE * off, Wd);
+    Sn.y = __shfl_down_sync(0xffffffffu, S.y, STRIDE * off, Wd);
+    if (j + off < RL) {
+      S = fma2(P, Sn, S);
+      P = mul2(P, Pn);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Asynchronous global -> shared copies (cp.async, 16 bytes; the bytes past
+// src_bytes are zero-filled and not read).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, int src_bytes) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem_dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gsrc),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// B / C chunk staging for the paired kernels.
+//
+// Raw copy: raw[2][kN][CH] elements of the I/O type (B rows then C rows of
+// the chunk [t0, t0 + CH) of one batch), filled by cp.async; steps at or
+// past L are zero.  Requires L % Io::kVec == 0 (16-byte aligned rows).
+//
+// Pair layout: float4 slot ((w * 8 + q) * (KT / 2) + k) * RL + j holds
+// (X[2q][t], X[2q+1][t], X[2q][t+1], X[2q+1][t+1]) with t = KT j + 2 k and
+// X = B (w = 0) or C (w = 1): lane j of a row reads its KT steps of the
+// state pair q as KT/2 conflict-free 128-bit loads.
+// ---------------------------------------------------------------------------
+template <typename Io, int CH>
+__device__ __forceinline__ void issue_raw_bc(const typename Io::T* __restrict__ Bb,
+                                             const typename Io::T* __restrict__ Cb, int64_t L,
+                                             int64_t t0, typename Io::T* raw, int tid, int nthr) {
+  using T = typename Io::T;
+  constexpr int V = Io::kVec;  // elements per 16 bytes
+  constexpr int per_row = CH / V;
+  constexpr int total = 2 * kN * per_row;
+  for (int i = tid; i < total; i += nthr) {
+    const int w = i / (kN * per_row);
+    const int rem = i - w * kN * per_row;
+    const int n = rem / per_row;
+    const int tl = (rem - n * per_row) * V;
+    const int64_t t = t0 + tl;
+    const T* row = (w ? Cb : Bb) + (int64_t)n * L;
+    const bool in = t < L;  // whole vector in or out: L % V == 0
+    cp_async16(raw + (w * kN + n) * CH + tl, in ? (const void*)(row + t) : (const void*)row,
+               in ? 16 : 0);
+  }
+}
+
+template <typename Io, int CH, int KT, int RL>
+__device__ __forceinline__ void raw_to_pairs(const typename Io::T* raw, float4* pairs, int tid,
+                                             int nthr) {
+  constexpr int items = 2 * (kN / 2) * (CH / 8);  // (w, q, octet of steps)
+  constexpr int m = KT / 8;                         // octets per lane segment
+  static_assert(CH / 8 == RL * m, "chunk = RL segments of KT steps");
+  for (int i = tid; i < items; i += nthr) {
+    // consecutive threads -> consecutive segments j at the same k: the four
+    // 16-byte stores of a quarter-warp fill one contiguous 128-byte line
+    const int x = i % (CH / 8);
+    const int o = m * (x % RL) + x / RL;
+    const int wq = i / (CH / 8);  // w * 8 + q
+    const int w = wq >> 3, q = wq & 7;
+    const typename Io::T* r0 = raw + (w * kN + 2 * q) * CH + 8 * o;
+    const typename Io::T* r1 = r0 + CH;
+    float v0[8], v1[8];
+    if constexpr (Io::kVec == 8) {
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(r0), v0);
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(r1), v1);
+    } else {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float4 a = *reinterpret_cast<const float4*>(r0 + 4 * h);
+        const float4 b = *reinterpret_cast<const float4*>(r1 + 4 * h);
+        v0[4 * h] = a.x; v0[4 * h + 1] = a.y; v0[4 * h + 2] = a.z; v0[4 * h + 3] = a.w;
+        v1[4 * h] = b.x; v1[4 * h + 1] = b.y; v1[4 * h + 2] = b.z; v1[4 * h + 3] = b.w;
+      }
+    }
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int t = 8 * o + 2 * s;
+      const int j = t / KT, k = (t % KT) / 2;
+      pairs[(wq * (KT / 2) + k) * RL + j] = make_float4(v0[2 * s], v1[2 * s], v0[2 * s + 1], v1[2 * s + 1]);
+    }
+  }
+}
+
+// Scalar (any L) version: read B/C of the chunk straight into the pair layout.
+template <typename Io, int CH, int KT, int RL>
+__device__ __forceinline__ void load_pairs_scalar(const typename Io::T* __restrict__ Bb,
+                                                  const typename Io::T* __restrict__ Cb, int64_t L,
+                                                  int64_t t0, float4* pairs, int tid, int nthr) {
+  constexpr int items = 2 * (kN / 2) * (CH / 2);  // (w, q, step pair)
+  for (int i = tid; i < items; i += nthr) {
+    const int k2 = i % (CH / 2);
+    const int wq = i / (CH / 2);
+    const int w = wq >> 3, q = wq & 7;
+    const int t = 2 * k2;
+    const typename Io::T* r0 = (w ? Cb : Bb) + (int64_t)(2 * q) * L;
+    const typename Io::T* r1 = r0 + L;
+    const int64_t ta = t0 + t, tb = ta + 1;
+    const float a0 = ta < L ? Io::to_f(r0[ta]) : 0.f, a1 = ta < L ? Io::to_f(r1[ta]) : 0.f;
+    const float b0 = tb < L ? Io::to_f(r0[tb]) : 0.f, b1 = tb < L ? Io::to_f(r1[tb]) : 0.f;
+    const int j = t / KT, k = (t % KT) / 2;
+    pairs[(wq * (KT / 2) + k) * RL + j] = make_float4(a0, a1, b0, b1);
+  }
+}
+
+// Load KT consecutive elements starting at t (KT % Io::kVec == 0) as float,
+// zero at or past L.  kVec: L % Io::kVec == 0, so each 16-byte vector is
+// wholly inside or outside [0, L).
+template <typename Io, int KT, bool kVec>
+__device__ __forceinline__ void load_kt(const typename Io::T* row, int64_t t, int64_t L, bool valid,
+                                        float (&v)[KT]) {
+  constexpr int V = Io::kVec;
+  if (kVec) {
+#pragma unroll
+    for (int q = 0; q < KT / V; ++q) {
+      const bool in = valid && (t + V * q < L);
+      uint4 w = in ? ldg_nc_v4(row + t + V * q) : make_uint4(0, 0, 0, 0);
+      if constexpr (V == 8) {
+        unpack_bf16x8(w, v + 8 * q);
+      } else {
+        v[4 * q] = __uint_as_float(w.x);
+        v[4 * q + 1] = __uint_as_float(w.y);
+        v[4 * q + 2] = __uint_as_float(w.z);
+        v[4 * q + 3] = __uint_as_float(w.w);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < KT; ++i) v[i] = (valid && t + i < L) ? Io::to_f(row[t + i]) : 0.f;
+  }
+}
+
+// Raw (undecoded) vector loads, for prefetching into registers.
+template <typename Io, int KT>
+struct RawSeg {
+  uint4 w[KT / Io::kVec];
+};
+
+template <typename Io, int KT>
+__device__ __forceinline__ void load_raw(const typename Io::T* row, int64_t t, int64_t L,
+                                         bool valid, RawSeg<Io, KT>& r) {
+  constexpr int V = Io::kVec;
+#pragma unroll
+  for (int q = 0; q < KT / V; ++q) {
+    const bool in = valid && (t + V * q < L);
+    r.w[q] = in ? ldg_nc_v4(row + t + V * q) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+template <typename Io, int KT>
+__device__ __forceinline__ void decode_raw(const RawSeg<Io, KT>& r, float (&v)[KT]) {
+  constexpr int V = Io::kVec;
+#pragma unroll
+  for (int q = 0; q < KT / V; ++q) {
+    if constexpr (V == 8) {
+      unpack_bf16x8(r.w[q], v + 8 * q);
+    } else {
+      v[4 * q] = __uint_as_float(r.w[q].x);
+      v[4 * q + 1] = __uint_as_float(r.w[q].y);
+      v[4 * q + 2] = __uint_as_float(r.w[q].z);
+      v[4 * q + 3] = __uint_as_float(r.w[q].w);
+    }
+  }
+}
+
+// Store KT values at row[t ..) (elements below L only).
+template <typename Io, int KT, bool kVec>
+__device__ __forceinline__ void store_kt(typename Io::T* row, int64_t t, int64_t L, bool valid,
+                                         const float (&v)[KT]) {
+  if (!valid) return;
+  constexpr int V = Io::kVec;
+  if (kVec) {
+#pragma unroll
+    for (int q = 0; q < KT / V; ++q) {
+      if (t + V * q >= L) continue;
+      uint4 w;
+      if constexpr (V == 8) {
+        w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+        w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+        w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+        w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+      } else {
+        w = make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
+                       __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3]));
+      }
+      stg_v4(row + t + V * q, w);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < KT; ++i)
+      if (t + i < L) row[t + i] = Io::from_f(v[i]);
+  }
+}
+
+}  // namespace selscan

@@ -1,4 +1,4 @@
-// Backward selective scan by recomputation.
+// Backward selective scan by recomputation, chunk-parallel.
 //
 // The official kernel's backward recomputes the forward's intermediates
 // instead of storing them ("mamba.py" page, gittoolsai.com, performance
@@ -12,422 +12,674 @@
 //   ddelta_t = sum_n lam_t[n] (A[n] a_t[n] h_{t-1}[n] + B_t[n] u_t)
 //   dA[n]   += sum lam_t[n] a_t[n] h_{t-1}[n] delta_t
 //   dB_t[n] += lam_t[n] delta_t u_t,  dC_t[n] += yhat_t h_t[n]   (sums over d)
-// with a_t h_{t-1} = h_t - b_t.
 //
-// Three kernels, all on the caller's stream:
-//  1. bwd_states: the forward scan without outputs, storing for every
-//     16-step lane segment its incoming state (workspace Hs).
-//  2. bwd_main: chunks in reverse order; per state n: replay h from Hs,
-//     reverse-fold the adjoint per lane, 16-lane reverse shuffle scan, replay
-//     the adjoint and form all products.  dB/dC are summed over the CTA's rows
-//     in shared memory and written as one partial per CTA (channel group);
-//     dA/dD/dbias as one partial per (batch, channel).
-//  3. bwd_reduce: sums the partials in a fixed order (deterministic results).
-// The three stages are launched by launch_scan_bwd(phase = 0, 1, 2).
+// The sequence is cut into chunks of kBwdChunk steps that are processed
+// independently once the state entering each chunk (forward) and the adjoint
+// entering it from the later chunk (reverse) are known:
+//  stage 0a  bwd_summary: one thread per (row, chunk) walks the chunk in time
+//            order with all 16 states in registers (no cross-lane traffic) and
+//            records the chunk's affine summaries: S = state at the chunk end
+//            from a zero start, Q = sum_t (prod_{k<=t} a_k) yhat_t C_t (the
+//            adjoint carry it sends back from a zero incoming carry), and
+//            sum_t delta_t (the decay over the chunk is exp(A sum delta)).
+//  stage 0b  bwd_carry: per (row, state), a walk over the chunks turns the
+//            summaries into the true incoming state h_in[c] and the incoming
+//            adjoint carry rho_in[c] = a lam at the first step of chunk c+1.
+//  stage 1   bwd_main: per (batch, chunk, block of 128 rows): per state pair,
+//            forward fold / 16-lane scan / replay for h, reverse fold / scan /
+//            replay for lam, and all products.  dB and dC are summed over the
+//            block's rows in shared memory (fixed order) and written as one
+//            partial per (batch, row block); dA, dD, dbias as one partial per
+//            (row, chunk).
+//  stage 2   bwd_reduce: fixed-order sums of the partials (results are
+//            bitwise reproducible).
 #include "common.cuh"
 #include "launch.h"
+
+#include <stdlib.h>
 
 namespace selscan {
 
 namespace {
 
-constexpr int kWf = 8;  // warps per CTA, state kernel
-constexpr int kWb = 8;  // warps per CTA, main kernel
+constexpr int kKTb = 8;                    // steps per lane (main kernel)
+constexpr int kRLb = 16;                   // lanes per row
+constexpr int kBwdChunk = kKTb * kRLb;     // 128 steps per chunk
+constexpr int kRowBlock = 128;             // rows per CTA (main kernel)
+constexpr int kSumThreads = 128;           // rows per CTA (summary kernel)
 
 struct WsLayout {
-  size_t hs, pbc, pa, pd, pbias, total;
-  int64_t nchunks, groups;
+  size_t sumS, sumQ, dsum, pbc, pa, pd, pbias, total;
+  int64_t nchunks, blocks;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 inline WsLayout ws_layout(int64_t Bsz, int64_t Dch, int64_t L) {
   WsLayout w;
-  w.nchunks = (L + kChunk - 1) / kChunk;
-  w.groups = (Dch + 2 * kWb - 1) / (2 * kWb);
+  w.nchunks = (L + kBwdChunk - 1) / kBwdChunk;
+  w.blocks = (Dch + kRowBlock - 1) / kRowBlock;
+  const size_t rc = (size_t)(Bsz * Dch) * w.nchunks;  // (row, chunk) pairs
   size_t off = 0;
-  w.hs = off;
-  off = align256(off + sizeof(float) * (size_t)(Bsz * Dch) * w.nchunks * kN * kRowLanes);
-  w.pbc = off;
-  off = align256(off + sizeof(float) * (size_t)w.groups * Bsz * 2 * kN * L);
-  w.pa = off;
-  off = align256(off + sizeof(float) * (size_t)(Bsz * Dch) * kN);
-  w.pd = off;
-  off = align256(off + sizeof(float) * (size_t)(Bsz * Dch));
-  w.pbias = off;
-  off = align256(off + sizeof(float) * (size_t)(Bsz * Dch));
+  w.sumS = off;  off = align256(off + sizeof(float) * rc * kN);
+  w.sumQ = off;  off = align256(off + sizeof(float) * rc * kN);
+  w.dsum = off;  off = align256(off + sizeof(float) * rc);
+  w.pbc = off;   off = align256(off + sizeof(float) * (size_t)(Bsz * w.blocks) * 2 * kN * L);
+  w.pa = off;    off = align256(off + sizeof(float) * rc * kN);
+  w.pd = off;    off = align256(off + sizeof(float) * rc);
+  w.pbias = off; off = align256(off + sizeof(float) * rc);
   w.total = off;
   return w;
 }
 
-// ---------------------------------------------------------------------------
-// 1. incoming state of every lane segment
-// ---------------------------------------------------------------------------
-template <typename Io, int W, bool kVec>
-__global__ void __launch_bounds__(W * 32) bwd_states_kernel(ScanArgs p, float* __restrict__ Hs) {
-  using T = typename Io::T;
-  constexpr int R = 2 * W;
-  constexpr int NT = W * 32;
-  extern __shared__ float4 smem4[];
-  float* Bs = reinterpret_cast<float*>(smem4);
-  float* carry = Bs + kN * kChunk;  // [2][R][kN]
-  float* A2s = carry + 2 * R * kN;  // [R][kN]
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int j = lane & 15;
-  const int r = 2 * warp + (lane >> 4);
-  const int64_t b = blockIdx.y;
-  const int64_t d0 = (int64_t)blockIdx.x * R;
-  const int64_t d = d0 + r;
-  const bool valid = d < p.Dch;
-  const int64_t L = p.L;
-  const int64_t row = b * p.Dch + (valid ? d : 0);
-  const int64_t nchunks = (L + kChunk - 1) / kChunk;
-
-  for (int i = tid; i < R * kN; i += NT) {
-    const int64_t dd = d0 + i / kN;
-    carry[i] = 0.f;
-    A2s[i] = dd < p.Dch ? p.A[dd * kN + i % kN] * kLog2e : 0.f;
-  }
-  const float bias = (valid && p.delta_bias) ? p.delta_bias[d] : 0.f;
-  const T* urow = static_cast<const T*>(p.u) + row * L;
-  const T* drow = static_cast<const T*>(p.delta) + row * L;
-  const T* Bb = static_cast<const T*>(p.B) + b * kN * L;
-
-  int cur = 0;
-  int64_t c = 0;
-  for (int64_t t0 = 0; t0 < L; t0 += kChunk, cur ^= 1, ++c) {
-    __syncthreads();
-    // stage B only (C is not needed here); reuse the generic stager with C = B
-    stage_bc<Io, kVec>(Bb, Bb, L, t0, Bs, Bs, tid, NT);
-    const int64_t ts = t0 + kT * j;
-    float dl[kT], du[kT];
-    load_seg<Io, kVec>(urow, ts, L, valid, du);
-    load_seg<Io, kVec>(drow, ts, L, valid, dl);
-    __syncthreads();
-    float dsum = 0.f;
-#pragma unroll
-    for (int i = 0; i < kT; ++i) {
-      const float x = dl[i] + bias;
-      float dt = p.softplus ? softplus_f(x) : x;
-      dt = (valid && ts + i < L) ? dt : 0.f;
-      dl[i] = dt;
-      du[i] = dt * du[i];
-      dsum += dt;
-    }
-    float* hs_out = Hs + ((row * nchunks + c) * kN) * kRowLanes + j;
-#pragma unroll 1
-    for (int n = 0; n < kN; ++n) {
-      const float a2 = A2s[r * kN + n];
-      const float hc = carry[(cur * R + r) * kN + n];
-      float v[kT];
-      read_bc(Bs, n, j, v);
-      float S = 0.f;
-#pragma unroll
-      for (int i = 0; i < kT; ++i) S = fmaf(ex2f(dl[i] * a2), S, du[i] * v[i]);
-      float P = ex2f(a2 * dsum);
-      scan16_fwd(P, S, j);
-      float Pe = __shfl_up_sync(0xffffffffu, P, 1, kRowLanes);
-      float Se = __shfl_up_sync(0xffffffffu, S, 1, kRowLanes);
-      if (j == 0) {
-        Pe = 1.f;
-        Se = 0.f;
-      }
-      if (valid) hs_out[n * kRowLanes] = fmaf(Pe, hc, Se);
-      if (j == kRowLanes - 1) carry[((cur ^ 1) * R + r) * kN + n] = fmaf(P, hc, S);
-    }
-  }
+// The discretised step delta = softplus(raw + bias) (or the raw sum).
+__device__ __forceinline__ float step_delta(float raw, float bias, int softplus) {
+  const float x = raw + bias;
+  return softplus ? softplus_fast(x) : x;
 }
 
 // ---------------------------------------------------------------------------
-// 2. reverse pass
+// 0a. chunk summaries
 // ---------------------------------------------------------------------------
-template <typename Io, int W, bool kVec>
-__global__ void __launch_bounds__(W * 32, 1)
-    bwd_main_kernel(ScanArgs p, BwdOut o, const float* __restrict__ Hs, float* __restrict__ pBC,
-                    float* __restrict__ pA, float* __restrict__ pD, float* __restrict__ pbias) {
+template <typename Io, bool kVec>
+__global__ void __launch_bounds__(kSumThreads)
+    bwd_summary_kernel(ScanArgs p, BwdOut o, int64_t nrb, float* __restrict__ sumS,
+                       float* __restrict__ sumQ, float* __restrict__ dsum_out) {
   using T = typename Io::T;
-  constexpr int R = 2 * W;
-  constexpr int NT = W * 32;
-  extern __shared__ float4 smem4[];
-  float* Bs = reinterpret_cast<float*>(smem4);  // [kN][kChunk]
-  float* Cs = Bs + kN * kChunk;                 // [kN][kChunk]
-  float* red = Cs + kN * kChunk;                // [2 parity][W][2 (dB, dC)][kChunk]
-  float* carry = red + 2 * W * 2 * kChunk;      // [2][R][kN] reverse carry
-  float* A2s = carry + 2 * R * kN;              // [R][kN]
-  float* Araw = A2s + R * kN;                   // [R][kN]
-  float* dAs = Araw + R * kN;                   // [R][kN]
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int j = lane & 15, half = lane >> 4;
-  const int r = 2 * warp + half;
+  constexpr int CH = kBwdChunk;
+  __shared__ float4 sB4[CH * kN / 4], sC4[CH * kN / 4];  // [t][n]
+  float* sB = reinterpret_cast<float*>(sB4);
+  float* sC = reinterpret_cast<float*>(sC4);
+  const int tid = threadIdx.x;
+  const int64_t c = blockIdx.x / nrb;
+  const int64_t rb = blockIdx.x - c * nrb;
   const int64_t b = blockIdx.y;
-  const int64_t g = blockIdx.x;
-  const int64_t d0 = g * R;
-  const int64_t d = d0 + r;
+  const int64_t d = rb * kSumThreads + tid;
   const bool valid = d < p.Dch;
-  const int64_t L = p.L;
-  const int64_t Bsz = p.Bsz;
+  const int64_t L = p.L, t0 = c * CH;
+  const int64_t nch = (L + CH - 1) / CH;
   const int64_t row = b * p.Dch + (valid ? d : 0);
-  const int64_t nchunks = (L + kChunk - 1) / kChunk;
 
-  for (int i = tid; i < R * kN; i += NT) {
-    const int64_t dd = d0 + i / kN;
-    const float av = dd < p.Dch ? p.A[dd * kN + i % kN] : 0.f;
-    carry[i] = 0.f;
-    A2s[i] = av * kLog2e;
-    Araw[i] = av;
-    dAs[i] = 0.f;
+  // stage B, C of (b, chunk) transposed to [t][n]
+  const T* Bb = static_cast<const T*>(p.B) + b * kN * L;
+  const T* Cb = static_cast<const T*>(p.C) + b * kN * L;
+  for (int i = tid; i < 2 * kN * (CH / 8); i += kSumThreads) {
+    // consecutive threads -> consecutive states n: the transposed [t][n]
+    // stores of a warp land in two 64-byte runs
+    const int n = i % kN;
+    const int wo = i / kN;
+    const int o = wo % (CH / 8), w = wo / (CH / 8);
+    const T* src = (w ? Cb : Bb) + (int64_t)n * L + t0 + 8 * o;
+    float v[8];
+    load_kt<Io, 8, kVec>(src, 0, L - t0 - 8 * o, true, v);
+    float* dst = (w ? sC : sB) + 8 * o * kN + n;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) dst[s * kN] = v[s];
   }
-  const float Dd = (valid && p.D) ? p.D[d] : 0.f;
-  const float bias = (valid && p.delta_bias) ? p.delta_bias[d] : 0.f;
+  __syncthreads();
+  if (!valid) return;
+
+  float A2[kN];
+#pragma unroll
+  for (int n = 0; n < kN; ++n) A2[n] = p.A[d * kN + n] * kLog2e;
+  const float bias = p.delta_bias ? p.delta_bias[d] : 0.f;
   const T* urow = static_cast<const T*>(p.u) + row * L;
   const T* drow = static_cast<const T*>(p.delta) + row * L;
   const T* zrow = p.z ? static_cast<const T*>(p.z) + row * L : nullptr;
   const T* grow = static_cast<const T*>(o.dy) + row * L;
-  T* du_row = static_cast<T*>(o.du) + row * L;
-  T* dd_row = static_cast<T*>(o.ddelta) + row * L;
-  T* dz_row = o.dz ? static_cast<T*>(o.dz) + row * L : nullptr;
+
+  float2 S[kN / 2], Q[kN / 2], cp[kN / 2];
+#pragma unroll
+  for (int q = 0; q < kN / 2; ++q) {
+    S[q] = make_float2(0.f, 0.f);
+    Q[q] = make_float2(0.f, 0.f);
+    cp[q] = make_float2(1.f, 1.f);
+  }
+  float dsum = 0.f;
+  // 8-step blocks; with 16-byte rows the next block's inputs are loaded while
+  // the current one is processed
+  RawSeg<Io, 8> nu, nd, nz, ng;
+  if (kVec) {
+    load_raw<Io, 8>(urow, t0, L, true, nu);
+    load_raw<Io, 8>(drow, t0, L, true, nd);
+    load_raw<Io, 8>(zrow, t0, L, zrow != nullptr, nz);
+    load_raw<Io, 8>(grow, t0, L, true, ng);
+  }
+#pragma unroll 1
+  for (int tb = 0; tb < CH; tb += 8) {
+    const int64_t t = t0 + tb;
+    float uu[8], dd[8], zz[8], gg[8];
+    if (kVec) {
+      decode_raw<Io, 8>(nu, uu);
+      decode_raw<Io, 8>(nd, dd);
+      decode_raw<Io, 8>(nz, zz);
+      decode_raw<Io, 8>(ng, gg);
+      if (tb + 8 < CH) {
+        load_raw<Io, 8>(urow, t + 8, L, true, nu);
+        load_raw<Io, 8>(drow, t + 8, L, true, nd);
+        load_raw<Io, 8>(zrow, t + 8, L, zrow != nullptr, nz);
+        load_raw<Io, 8>(grow, t + 8, L, true, ng);
+      }
+    } else {
+      load_kt<Io, 8, kVec>(urow, t, L, true, uu);
+      load_kt<Io, 8, kVec>(drow, t, L, true, dd);
+      load_kt<Io, 8, kVec>(zrow, t, L, zrow != nullptr, zz);
+      load_kt<Io, 8, kVec>(grow, t, L, true, gg);
+    }
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const bool in = t + s < L;
+      const float dt = in ? step_delta(dd[s], bias, p.softplus) : 0.f;
+      const float dtu = dt * uu[s];
+      const float yh = zrow ? gg[s] * zz[s] * sigmoid_f(zz[s]) : gg[s];
+      dsum += dt;
+      const float4* bq = reinterpret_cast<const float4*>(sB + (tb + s) * kN);
+      const float4* cq = reinterpret_cast<const float4*>(sC + (tb + s) * kN);
+#pragma unroll
+      for (int k = 0; k < kN / 4; ++k) {
+        const float4 bv = bq[k], cv = cq[k];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int q = 2 * k + h;
+          const float2 e = mul2(make_float2(dt, dt), make_float2(A2[2 * q], A2[2 * q + 1]));
+          const float2 a = make_float2(ex2f(e.x), ex2f(e.y));
+          const float2 bp = h ? make_float2(bv.z, bv.w) : make_float2(bv.x, bv.y);
+          const float2 cc = h ? make_float2(cv.z, cv.w) : make_float2(cv.x, cv.y);
+          S[q] = fma2(a, S[q], mul2(make_float2(dtu, dtu), bp));
+          cp[q] = mul2(cp[q], a);
+          Q[q] = fma2(cp[q], mul2(make_float2(yh, yh), cc), Q[q]);
+        }
+      }
+    }
+  }
+  const size_t rc = (size_t)row * nch + c;
+  float4* so = reinterpret_cast<float4*>(sumS + rc * kN);
+  float4* qo = reinterpret_cast<float4*>(sumQ + rc * kN);
+#pragma unroll
+  for (int k = 0; k < kN / 4; ++k) {
+    so[k] = make_float4(S[2 * k].x, S[2 * k].y, S[2 * k + 1].x, S[2 * k + 1].y);
+    qo[k] = make_float4(Q[2 * k].x, Q[2 * k].y, Q[2 * k + 1].x, Q[2 * k + 1].y);
+  }
+  dsum_out[rc] = dsum;
+}
+
+// ---------------------------------------------------------------------------
+// 0b. chunk carries: sumS[row][c] <- h entering chunk c; sumQ[row][c] <- the
+//     adjoint carry entering chunk c from chunk c+1 (zero for the last).
+// ---------------------------------------------------------------------------
+__global__ void bwd_carry_kernel(const float* __restrict__ A, int64_t Bsz, int64_t Dch,
+                                 int64_t nch, float* __restrict__ sumS, float* __restrict__ sumQ,
+                                 const float* __restrict__ dsum) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= Bsz * Dch * kN) return;
+  const int64_t row = i / kN;
+  const int n = (int)(i % kN);
+  const int64_t d = row % Dch;
+  const float a2 = A[d * kN + n] * kLog2e;
+  float h = 0.f;
+  for (int64_t c = 0; c < nch; ++c) {
+    const size_t rc = (size_t)row * nch + c;
+    const float P = ex2f(a2 * dsum[rc]);
+    const float s = sumS[rc * kN + n];
+    sumS[rc * kN + n] = h;
+    h = fmaf(P, h, s);
+  }
+  float rho = 0.f;
+  for (int64_t c = nch - 1; c >= 0; --c) {
+    const size_t rc = (size_t)row * nch + c;
+    const float P = ex2f(a2 * dsum[rc]);
+    const float qv = sumQ[rc * kN + n];
+    sumQ[rc * kN + n] = rho;
+    rho = fmaf(P, rho, qv);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 1. main reverse pass
+//
+// Lane layout: the two rows of a warp sit in adjacent lanes (lane = 2 j + rs,
+// j = 0..15 the time segment, rs the row), so the 128-bit reads of the B / C
+// pair layout, identical for both rows, are served once per lane pair.
+// Per state pair the lane runs: forward fold, 16-segment scan, replay (h_t,
+// qq_t = a_t h_{t-1}, pre-gate output, dC terms), reverse fold, scan, replay
+// (lam_t, dB terms, the du / ddelta sums over states, dA terms).  Every row
+// writes its dB / dC terms to its own slot; after a barrier the 256 threads
+// sum the 16 rows' slots into the block accumulator.
+// ---------------------------------------------------------------------------
+template <int W>
+struct MainSmem {
+  static constexpr int KT = kKTb, RL = kRLb, CH = kBwdChunk, R = 2 * W;
+  static constexpr size_t pairs = sizeof(float4) * 2 * (kN / 2) * (KT / 2) * RL;  // B, C
+  static constexpr size_t slot_row = 2 * 2 * CH + 4;  // [dB,dC][2][CH] floats, padded so the
+                                                      // two rows of a warp use other banks
+  static constexpr size_t slots = sizeof(float) * 2 * R * slot_row;     // [parity][row]
+  static constexpr size_t acc = sizeof(float) * 2 * kN * CH;            // [dB,dC][n][CH]
+  static constexpr size_t dA = sizeof(float) * R * kN * RL;             // [row][n][j]
+  static constexpr size_t params = sizeof(float) * 4 * R * kN;          // A2, A, h_in, rho_in
+  static constexpr size_t total = pairs + slots + acc + dA + params;
+};
+
+// Four consecutive steps' values of the two states as two float4 stores.
+__device__ __forceinline__ void store_pair4(float* lo, float* hi, float2 v0, float2 v1, float2 v2,
+                                            float2 v3) {
+  *reinterpret_cast<float4*>(lo) = make_float4(v0.x, v1.x, v2.x, v3.x);
+  *reinterpret_cast<float4*>(hi) = make_float4(v0.y, v1.y, v2.y, v3.y);
+}
+
+// One state pair q of one row: forward fold / scan / replay, reverse fold /
+// scan / replay and the products.  Accumulates the per-step sums over states
+// (pre-gate output, sum lam B, sum A lam a h) in the row's registers, stores
+// the row's dB and dC terms of the pair at dB_lo / dC_lo (state 2q, state 2q+1
+// at +CH) and the lane's dA terms of the two states at dA_lo[0], dA_lo[RL].
+template <int KT, int RL, int CH>
+__device__ __forceinline__ void bwd_state_pair(
+    int q, int j, int r, bool valid, const float* A2s, const float* Ars, const float* hin_row,
+    const float* rin_row, const float4* Bp, const float4* Cp, const float (&dl)[KT],
+    const float2 (&du2)[KT], const float2 (&yh2)[KT], float dsum, float2 (&yacc2)[KT],
+    float2 (&s12)[KT], float2 (&s22)[KT], float* dB_lo, float* dC_lo, float* dA_lo) {
+    const float2 a2 = *reinterpret_cast<const float2*>(A2s + r * kN + 2 * q);
+    const float2 Ar = *reinterpret_cast<const float2*>(Ars + r * kN + 2 * q);
+    const float2 hc = valid ? *reinterpret_cast<const float2*>(hin_row + 2 * q) : make_float2(0.f, 0.f);
+    const float2 rcar = valid ? *reinterpret_cast<const float2*>(rin_row + 2 * q) : make_float2(0.f, 0.f);
+    const float4* bq = Bp + q * (KT / 2) * RL + j;
+    const float4* cq = Cp + q * (KT / 2) * RL + j;
+
+    float2 a[KT], bb[KT], mu[KT];
+#pragma unroll
+    for (int k = 0; k < KT / 2; ++k) {
+      const float2 dd = make_float2(dl[2 * k], dl[2 * k + 1]);
+      const float2 e0 = mul2(dd, make_float2(a2.x, a2.x));
+      const float2 e1 = mul2(dd, make_float2(a2.y, a2.y));
+      a[2 * k] = make_float2(ex2f(e0.x), ex2f(e1.x));
+      a[2 * k + 1] = make_float2(ex2f(e0.y), ex2f(e1.y));
+      const float4 v = bq[k * RL];
+      bb[2 * k] = mul2(du2[2 * k], make_float2(v.x, v.y));
+      bb[2 * k + 1] = mul2(du2[2 * k + 1], make_float2(v.z, v.w));
+      const float4 cv = cq[k * RL];
+      mu[2 * k] = mul2(yh2[2 * k], make_float2(cv.x, cv.y));
+      mu[2 * k + 1] = mul2(yh2[2 * k + 1], make_float2(cv.z, cv.w));
+    }
+    const float2 ps = mul2(make_float2(dsum, dsum), a2);
+    const float2 Pseg = make_float2(ex2f(ps.x), ex2f(ps.y));
+
+    // The reverse fold needs only the decays and mu, not h: both folds and
+    // both segment scans run interleaved (two independent chains).
+    float2 S = bb[0], Lam = mu[KT - 1];
+#pragma unroll
+    for (int k = 0; k < KT - 1; ++k) {
+      S = fma2(a[k + 1], S, bb[k + 1]);
+      Lam = fma2(a[KT - 1 - k], Lam, mu[KT - 2 - k]);
+    }
+    float2 Qs = mul2(a[0], Lam);
+    float2 Pf = Pseg, Pr = Pseg;
+#pragma unroll
+    for (int off = 1; off < RL; off <<= 1) {
+      float2 Pp, Sp, Pn, Sn;
+      Pp.x = __shfl_up_sync(0xffffffffu, Pf.x, 2 * off);
+      Pp.y = __shfl_up_sync(0xffffffffu, Pf.y, 2 * off);
+      Sp.x = __shfl_up_sync(0xffffffffu, S.x, 2 * off);
+      Sp.y = __shfl_up_sync(0xffffffffu, S.y, 2 * off);
+      Pn.x = __shfl_down_sync(0xffffffffu, Pr.x, 2 * off);
+      Pn.y = __shfl_down_sync(0xffffffffu, Pr.y, 2 * off);
+      Sn.x = __shfl_down_sync(0xffffffffu, Qs.x, 2 * off);
+      Sn.y = __shfl_down_sync(0xffffffffu, Qs.y, 2 * off);
+      if (j >= off) {
+        S = fma2(Pf, Sp, S);
+        Pf = mul2(Pf, Pp);
+      }
+      if (j + off < RL) {
+        Qs = fma2(Pr, Sn, Qs);
+        Pr = mul2(Pr, Pn);
+      }
+    }
+    const float2 hout = fma2(Pf, hc, S);
+    const float2 rout = fma2(Pr, rcar, Qs);
+    float2 h, rin;
+    h.x = __shfl_up_sync(0xffffffffu, hout.x, 2);
+    h.y = __shfl_up_sync(0xffffffffu, hout.y, 2);
+    rin.x = __shfl_down_sync(0xffffffffu, rout.x, 2);
+    rin.y = __shfl_down_sync(0xffffffffu, rout.y, 2);
+    if (j == 0) h = hc;
+    if (j == RL - 1) rin = rcar;
+
+    // forward replay: h_t, qq_t = a_t h_{t-1}, pre-gate output, dC terms
+    float2 qq[KT];
+#pragma unroll
+    for (int k = 0; k < KT / 2; ++k) {
+      const float4 cv = cq[k * RL];
+      const float2 c0 = make_float2(cv.x, cv.y), c1 = make_float2(cv.z, cv.w);
+      qq[2 * k] = mul2(a[2 * k], h);
+      h = add2(qq[2 * k], bb[2 * k]);
+      yacc2[2 * k] = fma2(c0, h, yacc2[2 * k]);
+      bb[2 * k] = mul2(yh2[2 * k], h);  // dC term (bb is free now)
+      qq[2 * k + 1] = mul2(a[2 * k + 1], h);
+      h = add2(qq[2 * k + 1], bb[2 * k + 1]);
+      yacc2[2 * k + 1] = fma2(c1, h, yacc2[2 * k + 1]);
+      bb[2 * k + 1] = mul2(yh2[2 * k + 1], h);
+    }
+    store_pair4(dC_lo, dC_lo + CH, bb[0], bb[1], bb[2], bb[3]);
+    store_pair4(dC_lo + 4, dC_lo + CH + 4, bb[4], bb[5], bb[6], bb[7]);
+
+    // reverse replay: lam_t and the products
+    float2 lam = add2(mu[KT - 1], rin);
+    float2 dA2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = KT / 2 - 1; k >= 0; --k) {
+      const float4 bv = bq[k * RL];
+#pragma unroll
+      for (int e = 1; e >= 0; --e) {
+        const int i = 2 * k + e;
+        if (i < KT - 1) lam = fma2(a[i + 1], lam, mu[i]);
+        const float2 bp = e ? make_float2(bv.z, bv.w) : make_float2(bv.x, bv.y);
+        bb[i] = mul2(du2[i], lam);  // dB term
+        s12[i] = fma2(bp, lam, s12[i]);
+        const float2 lq = mul2(lam, qq[i]);
+        s22[i] = fma2(Ar, lq, s22[i]);
+        dA2 = fma2(make_float2(dl[i], dl[i]), lq, dA2);
+      }
+    }
+    store_pair4(dB_lo, dB_lo + CH, bb[0], bb[1], bb[2], bb[3]);
+    store_pair4(dB_lo + 4, dB_lo + CH + 4, bb[4], bb[5], bb[6], bb[7]);
+    dA_lo[0] = dA2.x;   // state 2q
+  dA_lo[RL] = dA2.y;  // state 2q + 1
+
+}
+
+template <typename Io, bool kVec, int W>
+__global__ void __launch_bounds__(W * 32)
+    bwd_main_kernel(ScanArgs p, BwdOut o, int64_t nrb, const float* __restrict__ Hin,
+                    const float* __restrict__ Rin, float* __restrict__ pBC,
+                    float* __restrict__ pA, float* __restrict__ pD, float* __restrict__ pbias) {
+  using T = typename Io::T;
+  using Sm = MainSmem<W>;
+  constexpr int KT = kKTb, RL = kRLb, CH = kBwdChunk, R = 2 * W, NT = W * 32;
+  constexpr int kPasses = kRowBlock / R;
+  constexpr int SR = (int)Sm::slot_row;
+  extern __shared__ float4 smem4[];
+  char* sm = reinterpret_cast<char*>(smem4);
+  float4* pairs = reinterpret_cast<float4*>(sm);
+  float* slots = reinterpret_cast<float*>(sm + Sm::pairs);
+  float* acc = reinterpret_cast<float*>(sm + Sm::pairs + Sm::slots);
+  float* dAs = reinterpret_cast<float*>(sm + Sm::pairs + Sm::slots + Sm::acc);
+  float* A2s = reinterpret_cast<float*>(sm + Sm::pairs + Sm::slots + Sm::acc + Sm::dA);
+  float* Ars = A2s + R * kN;
+  float* Hs = Ars + R * kN;   // [row][n] state entering the chunk
+  float* Rs = Hs + R * kN;    // [row][n] adjoint carry entering the chunk
+  const float4* Bp = pairs;
+  const float4* Cp = pairs + (kN / 2) * (KT / 2) * RL;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int j = lane >> 1, rs = lane & 1;
+  const int r = 2 * warp + rs;
+  const int64_t c = blockIdx.x / nrb;
+  const int64_t g = blockIdx.x - c * nrb;
+  const int64_t b = blockIdx.y;
+  const int64_t L = p.L, t0 = c * CH;
+  const int64_t nch = (L + CH - 1) / CH;
   const T* Bb = static_cast<const T*>(p.B) + b * kN * L;
   const T* Cb = static_cast<const T*>(p.C) + b * kN * L;
 
-  float dD_acc = 0.f, dbias_acc = 0.f;
-  int cur = 0;
-  for (int64_t c = nchunks - 1; c >= 0; --c, cur ^= 1) {
-    const int64_t t0 = c * kChunk;
+  if (kVec) {
+    // one-shot copy of the chunk's B / C, staged raw in the accumulator area
+    T* raw = reinterpret_cast<T*>(acc);
+    static_assert(2 * kN * CH * sizeof(T) <= Sm::acc, "raw staging must fit");
+    issue_raw_bc<Io, CH>(Bb, Cb, L, t0, raw, tid, NT);
+    cp_async_commit();
+    cp_async_wait_all();
     __syncthreads();
-    stage_bc<Io, kVec>(Bb, Cb, L, t0, Bs, Cs, tid, NT);
-    const int64_t ts = t0 + kT * j;
-    float dl[kT], du[kT], yh[kT], yacc[kT], s1[kT], s2[kT];
-    {
-      float uu[kT], zz[kT], gg[kT];
-      load_seg<Io, kVec>(urow, ts, L, valid, uu);
-      load_seg<Io, kVec>(drow, ts, L, valid, dl);
-      load_seg<Io, kVec>(zrow, ts, L, valid && zrow != nullptr, zz);
-      load_seg<Io, kVec>(grow, ts, L, valid, gg);
-#pragma unroll
-      for (int i = 0; i < kT; ++i) {
-        const float x = dl[i] + bias;
-        float dt = p.softplus ? softplus_f(x) : x;
-        dt = (valid && ts + i < L) ? dt : 0.f;
-        dl[i] = dt;
-        du[i] = dt * uu[i];
-        yh[i] = zrow ? gg[i] * zz[i] * sigmoid_f(zz[i]) : gg[i];
-        yacc[i] = Dd * uu[i];
-        dD_acc = fmaf(yh[i], uu[i], dD_acc);
-        s1[i] = 0.f;
-        s2[i] = 0.f;
-      }
-    }
-    float dsum = 0.f;
-#pragma unroll
-    for (int i = 0; i < kT; ++i) dsum += dl[i];
-    const float* hs_in = Hs + ((row * nchunks + c) * kN) * kRowLanes + j;
+    raw_to_pairs<Io, CH, KT, RL>(raw, pairs, tid, NT);
     __syncthreads();
+  } else {
+    load_pairs_scalar<Io, CH, KT, RL>(Bb, Cb, L, t0, pairs, tid, NT);
+  }
+  for (int i = tid; i < 2 * kN * CH; i += NT) acc[i] = 0.f;
+
+  const int64_t ts = t0 + KT * j;
+  float* my_slot0 = slots + (size_t)r * SR + KT * j;  // + parity * R * SR
+  // cross-row sum assignment: thread -> four consecutive floats of [dB,dC][2][CH]
+  const int sum_e = 4 * tid;                      // element of the row slot
+  const int sum_wh = sum_e / (2 * CH);            // 0: dB, 1: dC
+  const int sum_nl = (sum_e / CH) & 1;            // state within the pair
+  const int sum_t = sum_e % CH;
+  static_assert(4 * NT >= 2 * 2 * CH, "one float4 of the row slot per summing thread");
 
 #pragma unroll 1
-    for (int n = 0; n < kN; ++n) {
-      const float a2 = A2s[r * kN + n];
-      const float An = Araw[r * kN + n];
-      const float rc = carry[(cur * R + r) * kN + n];
-      float h = valid ? hs_in[n * kRowLanes] : 0.f;
-      float a[kT], hh[kT], qq[kT], v[kT];
-      read_bc(Bs, n, j, v);
-      // forward replay from the stored segment state
-#pragma unroll
-      for (int i = 0; i < kT; ++i) {
-        a[i] = ex2f(dl[i] * a2);
-        qq[i] = a[i] * h;              // a_t h_{t-1}
-        h = fmaf(du[i], v[i], qq[i]);  // h_t
-        hh[i] = h;
-      }
-      // reverse fold of the adjoint within the segment (zero incoming)
-      read_bc(Cs, n, j, v);
-      float Lam = yh[kT - 1] * v[kT - 1];
-#pragma unroll
-      for (int i = kT - 2; i >= 0; --i) Lam = fmaf(a[i + 1], Lam, yh[i] * v[i]);
-      float P = ex2f(a2 * dsum);
-      float Q = a[0] * Lam;
-      scan16_rev(P, Q, j);
-      float Pe = __shfl_down_sync(0xffffffffu, P, 1, kRowLanes);
-      float Qe = __shfl_down_sync(0xffffffffu, Q, 1, kRowLanes);
-      if (j == kRowLanes - 1) {
-        Pe = 1.f;
-        Qe = 0.f;
-      }
-      const float rho_in = fmaf(Pe, rc, Qe);
-      // products; dC, dB per time step, s1/s2/dA accumulations
-      float dAn = 0.f;
-      float dBv[kT], dCv[kT];
-      float lam = 0.f;
-#pragma unroll
-      for (int i = kT - 1; i >= 0; --i) {
-        const float mu = yh[i] * v[i];
-        yacc[i] = fmaf(v[i], hh[i], yacc[i]);
-        lam = (i == kT - 1) ? (mu + rho_in) : fmaf(a[i + 1], lam, mu);
-        dCv[i] = yh[i] * hh[i];
-        dBv[i] = lam * du[i];
-        const float lq = lam * qq[i];
-        s2[i] = fmaf(An, lq, s2[i]);
-        dAn = fmaf(dl[i], lq, dAn);
-        qq[i] = lam;  // keep lam_t for the B products below
-      }
-      if (j == 0) carry[((cur ^ 1) * R + r) * kN + n] = a[0] * qq[0];
-      read_bc(Bs, n, j, v);
-#pragma unroll
-      for (int i = 0; i < kT; ++i) s1[i] = fmaf(qq[i], v[i], s1[i]);
+  for (int pass = 0; pass < kPasses; ++pass) {
+    const int64_t d0 = g * kRowBlock + pass * R;
+    if (d0 >= p.Dch) break;  // uniform over the CTA
+    const int64_t d = d0 + r;
+    const bool valid = d < p.Dch;
+    const int64_t row = b * p.Dch + (valid ? d : 0);
+    __syncthreads();  // previous pass done with the per-pass buffers
+    for (int i = tid; i < R * kN; i += NT) {
+      const int64_t dd = d0 + i / kN;
+      const bool ok = dd < p.Dch;
+      const float av = ok ? p.A[dd * kN + i % kN] : 0.f;
+      A2s[i] = av * kLog2e;
+      Ars[i] = av;
+      const size_t rci = ((size_t)(b * p.Dch + (ok ? dd : 0)) * nch + c) * kN + i % kN;
+      Hs[i] = ok ? Hin[rci] : 0.f;
+      Rs[i] = ok ? Rin[rci] : 0.f;
+    }
+    __syncthreads();
 
-      // dA: sum over the 16 lanes of the row
-#pragma unroll
-      for (int off = 8; off >= 1; off >>= 1) dAn += __shfl_xor_sync(0xffffffffu, dAn, off);
-      if (j == 0) dAs[r * kN + n] += dAn;
+    const float Dd = (valid && p.D) ? p.D[d] : 0.f;
+    const float bias = (valid && p.delta_bias) ? p.delta_bias[d] : 0.f;
+    const T* urow = static_cast<const T*>(p.u) + row * L;
+    const T* drow = static_cast<const T*>(p.delta) + row * L;
+    const T* zrow = p.z ? static_cast<const T*>(p.z) + row * L : nullptr;
+    const T* grow = static_cast<const T*>(o.dy) + row * L;
+    const size_t rc = (size_t)row * nch + c;
+    const float* hin_row = Hs + r * kN;
+    const float* rin_row = Rs + r * kN;
 
-      // dB, dC: add the two rows of the warp, then sum over warps in smem
-      float* slot = red + ((size_t)((n & 1) * W + warp) * 2) * kChunk;
+    float dl[KT];
+    float2 du2[KT], yh2[KT], yacc2[KT], s12[KT], s22[KT];
+    float dD_acc = 0.f, dsum = 0.f;
+    {
+      float uu[KT], zz[KT], gg[KT];
+      load_kt<Io, KT, kVec>(urow, ts, L, valid, uu);
+      load_kt<Io, KT, kVec>(drow, ts, L, valid, dl);
+      load_kt<Io, KT, kVec>(zrow, ts, L, valid && zrow != nullptr, zz);
+      load_kt<Io, KT, kVec>(grow, ts, L, valid, gg);
 #pragma unroll
-      for (int i = 0; i < kT / 2; ++i) {
-        const float sb = half ? dBv[i] : dBv[i + kT / 2];
-        const float sc = half ? dCv[i] : dCv[i + kT / 2];
-        const float rb = __shfl_xor_sync(0xffffffffu, sb, 16);
-        const float rcv = __shfl_xor_sync(0xffffffffu, sc, 16);
-        dBv[i] = (half ? dBv[i + kT / 2] : dBv[i]) + rb;
-        dCv[i] = (half ? dCv[i + kT / 2] : dCv[i]) + rcv;
+      for (int i = 0; i < KT; ++i) {
+        const bool in = valid && ts + i < L;
+        const float dt = in ? step_delta(dl[i], bias, p.softplus) : 0.f;
+        const float yh = in ? (zrow ? gg[i] * zz[i] * sigmoid_f(zz[i]) : gg[i]) : 0.f;
+        dl[i] = dt;
+        du2[i] = make_float2(dt * uu[i], dt * uu[i]);
+        yh2[i] = make_float2(yh, yh);
+        yacc2[i] = make_float2(Dd * uu[i], 0.f);
+        s12[i] = make_float2(0.f, 0.f);
+        s22[i] = make_float2(0.f, 0.f);
+        dD_acc = fmaf(yh, uu[i], dD_acc);
+        dsum += dt;
       }
-      const int tl0 = kT * j + half * (kT / 2);
-#pragma unroll
-      for (int q4 = 0; q4 < kT / 8; ++q4) {
-        *reinterpret_cast<float4*>(slot + tl0 + 4 * q4) =
-            make_float4(dBv[4 * q4], dBv[4 * q4 + 1], dBv[4 * q4 + 2], dBv[4 * q4 + 3]);
-        *reinterpret_cast<float4*>(slot + kChunk + tl0 + 4 * q4) =
-            make_float4(dCv[4 * q4], dCv[4 * q4 + 1], dCv[4 * q4 + 2], dCv[4 * q4 + 3]);
-      }
+    }
+
+#pragma unroll 1
+    for (int q = 0; q < kN / 2; ++q) {
+      float* slot = my_slot0 + (size_t)(q & 1) * R * SR;
+      bwd_state_pair<KT, RL, CH>(q, j, r, valid, A2s, Ars, hin_row, rin_row, Bp, Cp, dl, du2, yh2,
+                                 dsum, yacc2, s12, s22, slot, slot + 2 * CH,
+                                 dAs + (r * kN + 2 * q) * RL + j);
+
+      // dB / dC of this state pair: sum the rows' slots into the accumulator
       __syncthreads();
-      for (int i = tid; i < 2 * kChunk; i += NT) {
-        const int q = i / kChunk, tl = i % kChunk;
-        const float* col = red + ((size_t)((n & 1) * W) * 2 + q) * kChunk + tl;
-        float acc = 0.f;
+      if (tid < 2 * 2 * CH / 4) {
+        const float* base = slots + (size_t)(q & 1) * R * SR + sum_e;
+        float4 sacc = *reinterpret_cast<const float4*>(base);
 #pragma unroll
-        for (int w = 0; w < W; ++w) acc += col[(size_t)w * 2 * kChunk];
-        if (t0 + tl < L) pBC[(((g * Bsz + b) * 2 + q) * kN + n) * L + t0 + tl] = acc;
+        for (int rr = 1; rr < R; ++rr) {
+          const float4 v = *reinterpret_cast<const float4*>(base + (size_t)rr * SR);
+          sacc.x += v.x; sacc.y += v.y; sacc.z += v.z; sacc.w += v.w;
+        }
+        float4* ap = reinterpret_cast<float4*>(acc + ((size_t)sum_wh * kN + 2 * q + sum_nl) * CH + sum_t);
+        float4 av = *ap;
+        av.x += sacc.x; av.y += sacc.y; av.z += sacc.z; av.w += sacc.w;
+        *ap = av;
       }
     }
 
     // per-time-step outputs
     {
-      float uu[kT], dr[kT], zz[kT], gg[kT], o1[kT], o2[kT], o3[kT];
-      load_seg<Io, kVec>(urow, ts, L, valid, uu);
-      load_seg<Io, kVec>(drow, ts, L, valid, dr);
-      load_seg<Io, kVec>(zrow, ts, L, valid && zrow != nullptr, zz);
-      load_seg<Io, kVec>(grow, ts, L, valid, gg);
+      float uu[KT], dr[KT], zz[KT], gg[KT], o1[KT], o2[KT], o3[KT];
+      load_kt<Io, KT, kVec>(urow, ts, L, valid, uu);
+      load_kt<Io, KT, kVec>(drow, ts, L, valid, dr);
+      load_kt<Io, KT, kVec>(zrow, ts, L, valid && zrow != nullptr, zz);
+      load_kt<Io, KT, kVec>(grow, ts, L, valid, gg);
+      float dbias_acc = 0.f;
 #pragma unroll
-      for (int i = 0; i < kT; ++i) {
-        o1[i] = fmaf(yh[i], Dd, dl[i] * s1[i]);  // du
-        const float ddt = fmaf(uu[i], s1[i], s2[i]);
+      for (int i = 0; i < KT; ++i) {
+        const float s1 = s12[i].x + s12[i].y;
+        const float s2 = s22[i].x + s22[i].y;
+        const float yacc = yacc2[i].x + yacc2[i].y;
+        o1[i] = fmaf(yh2[i].x, Dd, dl[i] * s1);  // du
+        const float ddt = fmaf(uu[i], s1, s2);
         const float ddr = p.softplus ? ddt * sigmoid_f(dr[i] + bias) : ddt;
         o2[i] = ddr;
         dbias_acc += (valid && ts + i < L) ? ddr : 0.f;
         if (zrow) {
           const float s = sigmoid_f(zz[i]);
-          o3[i] = gg[i] * yacc[i] * s * fmaf(zz[i], 1.f - s, 1.f);
+          o3[i] = gg[i] * yacc * s * fmaf(zz[i], 1.f - s, 1.f);
         } else {
           o3[i] = 0.f;
         }
       }
-      store_seg<Io, kVec>(du_row, ts, L, valid, o1);
-      store_seg<Io, kVec>(dd_row, ts, L, valid, o2);
-      if (dz_row) store_seg<Io, kVec>(dz_row, ts, L, valid, o3);
-    }
-  }
-
+      store_kt<Io, KT, kVec>(static_cast<T*>(o.du) + row * L, ts, L, valid, o1);
+      store_kt<Io, KT, kVec>(static_cast<T*>(o.ddelta) + row * L, ts, L, valid, o2);
+      if (o.dz) store_kt<Io, KT, kVec>(static_cast<T*>(o.dz) + row * L, ts, L, valid, o3);
 #pragma unroll
-  for (int off = 8; off >= 1; off >>= 1) {
-    dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, off);
-    dbias_acc += __shfl_xor_sync(0xffffffffu, dbias_acc, off);
+      for (int off = 2; off < 32; off <<= 1) {  // the row's 16 lanes (same parity)
+        dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, off);
+        dbias_acc += __shfl_xor_sync(0xffffffffu, dbias_acc, off);
+      }
+      if (valid && j == 0) {
+        pD[rc] = dD_acc;
+        pbias[rc] = dbias_acc;
+      }
+    }
+    // dA of the pass's rows: thread -> (row, state), sum over the 16 segments
+    __syncthreads();
+    for (int i = tid; i < R * kN; i += NT) {
+      const int rr = i / kN, n = i % kN;
+      const int64_t dd = d0 + rr;
+      const float4* src = reinterpret_cast<const float4*>(dAs + (rr * kN + n) * RL);
+      float sd = 0.f;
+#pragma unroll
+      for (int k4 = 0; k4 < RL / 4; ++k4) {
+        const float4 v = src[k4];
+        sd += (v.x + v.y) + (v.z + v.w);
+      }
+      if (dd < p.Dch) pA[((size_t)(b * p.Dch + dd) * nch + c) * kN + n] = sd;
+    }
   }
   __syncthreads();
-  if (valid) {
-    if (j == 0) {
-      pD[row] = dD_acc;
-      pbias[row] = dbias_acc;
-    }
-    pA[row * kN + j] = dAs[r * kN + j];
+  // this block's dB / dC partial for the chunk
+  float* out = pBC + ((size_t)(b * nrb + g) * 2) * kN * L;
+  for (int i = tid; i < 2 * kN * CH; i += NT) {
+    const int whn = i / CH, tt = i % CH;  // (wh * kN + n, t)
+    if (t0 + tt < L) out[(size_t)whn * L + t0 + tt] = acc[i];
   }
 }
 
 // ---------------------------------------------------------------------------
-// 3. fixed-order reduction of the partials
+// 2. fixed-order reduction of the partials
 // ---------------------------------------------------------------------------
-__global__ void bwd_reduce_bc_kernel(const float* __restrict__ pBC, int64_t groups, int64_t Bsz,
+__global__ void bwd_reduce_bc_kernel(const float* __restrict__ pBC, int64_t nrb, int64_t Bsz,
                                      int64_t L, float* __restrict__ dB, float* __restrict__ dC) {
   const int64_t per = Bsz * kN * L;  // elements of dB (and of dC)
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= 2 * per) return;
-  const int64_t q = i / per, e = i % per;  // e = (b * kN + n) * L + t
+  const int64_t wh = i / per, e = i % per;  // e = (b * kN + n) * L + t
   const int64_t b = e / (kN * L), nt = e % (kN * L);
   float acc = 0.f;
-  for (int64_t g = 0; g < groups; ++g) acc += pBC[((g * Bsz + b) * 2 + q) * kN * L + nt];
-  (q ? dC : dB)[e] = acc;
+  for (int64_t g = 0; g < nrb; ++g) acc += pBC[((b * nrb + g) * 2 + wh) * kN * L + nt];
+  (wh ? dC : dB)[e] = acc;
 }
 
 __global__ void bwd_reduce_param_kernel(const float* __restrict__ pA, const float* __restrict__ pD,
                                         const float* __restrict__ pbias, int64_t Bsz, int64_t Dch,
-                                        float* __restrict__ dA, float* __restrict__ dD,
+                                        int64_t nch, float* __restrict__ dA, float* __restrict__ dD,
                                         float* __restrict__ dbias) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i < Dch * kN) {
+    const int64_t d = i / kN, n = i % kN;
     float acc = 0.f;
-    for (int64_t b = 0; b < Bsz; ++b) acc += pA[b * Dch * kN + i];
+    for (int64_t b = 0; b < Bsz; ++b)
+      for (int64_t c = 0; c < nch; ++c) acc += pA[((b * Dch + d) * nch + c) * kN + n];
     dA[i] = acc;
   }
   if (i < Dch) {
     float a1 = 0.f, a2 = 0.f;
-    for (int64_t b = 0; b < Bsz; ++b) {
-      a1 += pD[b * Dch + i];
-      a2 += pbias[b * Dch + i];
-    }
+    for (int64_t b = 0; b < Bsz; ++b)
+      for (int64_t c = 0; c < nch; ++c) {
+        a1 += pD[(b * Dch + i) * nch + c];
+        a2 += pbias[(b * Dch + i) * nch + c];
+      }
     if (dD) dD[i] = a1;
     if (dbias) dbias[i] = a2;
   }
+}
+
+// Variant selector for experiments (0 = default).
+int bwd_variant() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("SELSCAN_BWD_VARIANT");
+    v = e ? atoi(e) : 0;
+  }
+  return v;
+}
+
+template <typename Io, bool kVec, int W>
+cudaError_t launch_main(const ScanArgs& a, const BwdOut& o, const WsLayout& w, float* sumS,
+                        float* sumQ, float* pBC, float* pA, float* pD, float* pbias,
+                        cudaStream_t s) {
+  using Sm = MainSmem<W>;
+  auto kern = bwd_main_kernel<Io, kVec, W>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sm::total);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)(w.blocks * w.nchunks), (unsigned)a.Bsz);
+  kern<<<grid, W * 32, Sm::total, s>>>(a, o, w.blocks, sumS, sumQ, pBC, pA, pD, pbias);
+  return cudaGetLastError();
 }
 
 template <typename Io, bool kVec>
 cudaError_t launch_bwd_t(int phase, const ScanArgs& a, const BwdOut& o, void* ws, cudaStream_t s) {
   const WsLayout w = ws_layout(a.Bsz, a.Dch, a.L);
   char* base = static_cast<char*>(ws);
-  float* Hs = reinterpret_cast<float*>(base + w.hs);
+  float* sumS = reinterpret_cast<float*>(base + w.sumS);
+  float* sumQ = reinterpret_cast<float*>(base + w.sumQ);
+  float* dsum = reinterpret_cast<float*>(base + w.dsum);
   float* pBC = reinterpret_cast<float*>(base + w.pbc);
   float* pA = reinterpret_cast<float*>(base + w.pa);
   float* pD = reinterpret_cast<float*>(base + w.pd);
   float* pbias = reinterpret_cast<float*>(base + w.pbias);
   cudaError_t e;
   if (phase == 0) {
-    constexpr int R = 2 * kWf;
-    const size_t smem = sizeof(float) * (kN * kChunk + 3 * R * kN);
-    auto kern = bwd_states_kernel<Io, kWf, kVec>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)((a.Dch + R - 1) / R), (unsigned)a.Bsz);
-    kern<<<grid, kWf * 32, smem, s>>>(a, Hs);
+    const int64_t nrb = (a.Dch + kSumThreads - 1) / kSumThreads;
+    dim3 grid((unsigned)(nrb * w.nchunks), (unsigned)a.Bsz);
+    bwd_summary_kernel<Io, kVec><<<grid, kSumThreads, 0, s>>>(a, o, nrb, sumS, sumQ, dsum);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int64_t n = a.Bsz * a.Dch * kN;
+    bwd_carry_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a.A, a.Bsz, a.Dch, w.nchunks,
+                                                                 sumS, sumQ, dsum);
     return cudaGetLastError();
   }
   if (phase == 1) {
-    constexpr int R = 2 * kWb;
-    const size_t smem =
-        sizeof(float) * (2 * kN * kChunk + 2 * kWb * 2 * kChunk + 2 * R * kN + 3 * R * kN);
-    auto kern = bwd_main_kernel<Io, kWb, kVec>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)w.groups, (unsigned)a.Bsz);
-    kern<<<grid, kWb * 32, smem, s>>>(a, o, Hs, pBC, pA, pD, pbias);
-    return cudaGetLastError();
+    return bwd_variant() == 1 ? launch_main<Io, kVec, 8>(a, o, w, sumS, sumQ, pBC, pA, pD, pbias, s)
+                              : launch_main<Io, kVec, 4>(a, o, w, sumS, sumQ, pBC, pA, pD, pbias, s);
   }
   const int64_t n = 2 * a.Bsz * kN * a.L;
-  bwd_reduce_bc_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(pBC, w.groups, a.Bsz, a.L,
+  bwd_reduce_bc_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(pBC, w.blocks, a.Bsz, a.L,
                                                                      o.dB, o.dC);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t m = a.Dch * kN;
   bwd_reduce_param_kernel<<<(unsigned)((m + 255) / 256), 256, 0, s>>>(
-      pA, pD, pbias, a.Bsz, a.Dch, o.dA, o.dD, o.ddelta_bias);
+      pA, pD, pbias, a.Bsz, a.Dch, w.nchunks, o.dA, o.dD, o.ddelta_bias);
   return cudaGetLastError();
 }
 

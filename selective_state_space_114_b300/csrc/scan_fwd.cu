@@ -16,6 +16,8 @@
 #include "common.cuh"
 #include "launch.h"
 
+#include <stdlib.h>
+
 namespace selscan {
 
 template <typename Io, int W, bool kVec>
@@ -121,6 +123,213 @@ __global__ void __launch_bounds__(W * 32)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Paired-state kernel (rows whose length is a multiple of the 16-byte vector).
+//
+// RL = 16 lanes per row, KT steps per lane, two rows per warp in adjacent
+// lanes (lane = 2 j + row), so that both rows' 128-bit reads of the shared
+// B / C tiles, identical addresses, are served once; every state update
+// handles the pair of states (2q, 2q+1) with
+// one packed f32x2 instruction, B and C arrive by cp.async one chunk ahead
+// (double-buffered raw copy, converted once per CTA into the pair layout),
+// and u / delta of the next chunk are prefetched into registers while the
+// current chunk is scanned.
+// ---------------------------------------------------------------------------
+template <typename Io, int W, int KT, bool kSplit = false>
+struct FwdPairCfg {
+  static constexpr int RL = 16;
+  static constexpr int R = 2 * W;
+  static constexpr int NT = W * 32;
+  static constexpr int CH = KT * RL;
+  static constexpr size_t raw_bytes = 2ull * kN * CH * sizeof(typename Io::T);
+  static constexpr size_t pair_bytes = 2ull * kN * CH * sizeof(float);
+  // raw[2] | pairs | carry[2][R][kN] | A2[R][kN]
+  static constexpr size_t smem = 2 * raw_bytes + pair_bytes + sizeof(float) * 3 * R * kN;
+};
+
+template <typename Io, int W, int KT, bool kSplit>
+__global__ void __launch_bounds__(W * 32)
+    scan_fwd_pair_kernel(ScanArgs p, typename Io::T* __restrict__ y_out, float* __restrict__ h_last) {
+  using T = typename Io::T;
+  using Cfg = FwdPairCfg<Io, W, KT>;
+  constexpr int H = KT / 2;
+  constexpr int RL = Cfg::RL, R = Cfg::R, NT = Cfg::NT, CH = Cfg::CH;
+  extern __shared__ float4 smem4[];
+  T* raw0 = reinterpret_cast<T*>(smem4);
+  T* raw1 = reinterpret_cast<T*>(reinterpret_cast<char*>(smem4) + Cfg::raw_bytes);
+  float4* pairs = reinterpret_cast<float4*>(reinterpret_cast<char*>(smem4) + 2 * Cfg::raw_bytes);
+  float* carry = reinterpret_cast<float*>(reinterpret_cast<char*>(pairs) + Cfg::pair_bytes);
+  float* A2s = carry + 2 * R * kN;
+  const float4* Bp = pairs;
+  const float4* Cp = pairs + kN / 2 * (KT / 2) * RL;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int j = lane >> 1;
+  const int r = 2 * warp + (lane & 1);
+  const int64_t b = blockIdx.y;
+  const int64_t d0 = (int64_t)blockIdx.x * R;
+  const int64_t d = d0 + r;
+  const bool valid = d < p.Dch;
+  const int64_t L = p.L;
+  const int64_t row = b * p.Dch + (valid ? d : 0);
+
+  for (int i = tid; i < R * kN; i += NT) {
+    const int64_t dd = d0 + i / kN;
+    carry[i] = 0.f;
+    A2s[i] = dd < p.Dch ? p.A[dd * kN + i % kN] * kLog2e : 0.f;
+  }
+  const float Dd = (valid && p.D) ? p.D[d] : 0.f;
+  const float bias = (valid && p.delta_bias) ? p.delta_bias[d] : 0.f;
+  const T* urow = static_cast<const T*>(p.u) + row * L;
+  const T* drow = static_cast<const T*>(p.delta) + row * L;
+  const T* zrow = p.z ? static_cast<const T*>(p.z) + row * L : nullptr;
+  T* yrow = y_out + row * L;
+  const T* Bb = static_cast<const T*>(p.B) + b * kN * L;
+  const T* Cb = static_cast<const T*>(p.C) + b * kN * L;
+  static_assert(RL == 16, "two interleaved rows of 16 segments per warp");
+
+  // prologue: chunk 0's B/C copy and u/delta registers
+  issue_raw_bc<Io, CH>(Bb, Cb, L, 0, raw0, tid, NT);
+  cp_async_commit();
+  RawSeg<Io, KT> ru, rd;
+  load_raw<Io, KT>(urow, KT * j, L, valid, ru);
+  load_raw<Io, KT>(drow, KT * j, L, valid, rd);
+
+  int cur = 0;
+  for (int64_t t0 = 0; t0 < L; t0 += CH, cur ^= 1) {
+    cp_async_wait_all();
+    __syncthreads();  // raw[cur] landed for all threads; pairs free; carry visible
+    raw_to_pairs<Io, CH, KT, RL>(cur ? raw1 : raw0, pairs, tid, NT);
+    if (t0 + CH < L) issue_raw_bc<Io, CH>(Bb, Cb, L, t0 + CH, cur ? raw0 : raw1, tid, NT);
+    cp_async_commit();
+    __syncthreads();  // pairs ready
+
+    const int64_t ts = t0 + KT * j;
+    float dl[KT], du[KT], y[KT];
+    decode_raw<Io, KT>(ru, du);
+    decode_raw<Io, KT>(rd, dl);
+    RawSeg<Io, KT> rz;
+    load_raw<Io, KT>(zrow, ts, L, valid && zrow != nullptr, rz);
+    load_raw<Io, KT>(urow, ts + CH, L, valid, ru);  // next chunk
+    load_raw<Io, KT>(drow, ts + CH, L, valid, rd);
+
+    float dsum = 0.f, dlo = 0.f;
+#pragma unroll
+    for (int i = 0; i < KT; ++i) {
+      const float x = dl[i] + bias;
+      float dt = p.softplus ? softplus_fast(x) : x;
+      dt = (valid && ts + i < L) ? dt : 0.f;
+      dl[i] = dt;
+      y[i] = Dd * du[i];
+      du[i] = dt * du[i];
+      dsum += dt;
+      if (i == H - 1) dlo = dsum;
+    }
+
+#pragma unroll 1
+    for (int q = 0; q < kN / 2; ++q) {
+      const float2 a2 = *reinterpret_cast<const float2*>(A2s + r * kN + 2 * q);
+      const float2 hc = *reinterpret_cast<const float2*>(carry + (cur * R + r) * kN + 2 * q);
+      const float4* bq = Bp + q * (KT / 2) * RL + j;
+      const float4* cq = Cp + q * (KT / 2) * RL + j;
+      float2 a[KT], bb[KT], hout;
+#pragma unroll
+      for (int k = 0; k < KT / 2; ++k) {
+        const float2 dd = make_float2(dl[2 * k], dl[2 * k + 1]);
+        const float2 e0 = mul2(dd, make_float2(a2.x, a2.x));
+        const float2 e1 = mul2(dd, make_float2(a2.y, a2.y));
+        a[2 * k] = make_float2(ex2f(e0.x), ex2f(e1.x));
+        a[2 * k + 1] = make_float2(ex2f(e0.y), ex2f(e1.y));
+        const float4 v = bq[k * RL];
+        bb[2 * k] = make_float2(du[2 * k] * v.x, du[2 * k] * v.y);
+        bb[2 * k + 1] = make_float2(du[2 * k + 1] * v.z, du[2 * k + 1] * v.w);
+      }
+      if constexpr (!kSplit) {
+        float2 S = bb[0];
+#pragma unroll
+        for (int i = 1; i < KT; ++i) S = fma2(a[i], S, bb[i]);
+        const float2 ps = mul2(make_float2(dsum, dsum), a2);
+        float2 P = make_float2(ex2f(ps.x), ex2f(ps.y));
+        scan_pair_fwd<RL, 2>(P, S, j);
+        hout = fma2(P, hc, S);  // state after this lane's segment
+        float2 h;
+        h.x = __shfl_up_sync(0xffffffffu, hout.x, 2);
+        h.y = __shfl_up_sync(0xffffffffu, hout.y, 2);
+        if (j == 0) h = hc;
+#pragma unroll
+        for (int k = 0; k < KT / 2; ++k) {
+          const float4 c = cq[k * RL];
+          h = fma2(a[2 * k], h, bb[2 * k]);
+          y[2 * k] = fmaf(c.y, h.y, fmaf(c.x, h.x, y[2 * k]));
+          h = fma2(a[2 * k + 1], h, bb[2 * k + 1]);
+          y[2 * k + 1] = fmaf(c.w, h.y, fmaf(c.z, h.x, y[2 * k + 1]));
+        }
+      } else {
+        // two half-segment folds and replays, run side by side
+        float2 Slo = bb[0], Shi = bb[H];
+#pragma unroll
+        for (int i = 1; i < H; ++i) {
+          Slo = fma2(a[i], Slo, bb[i]);
+          Shi = fma2(a[H + i], Shi, bb[H + i]);
+        }
+        const float2 pl = mul2(make_float2(dlo, dlo), a2);
+        const float2 ph = mul2(make_float2(dsum - dlo, dsum - dlo), a2);
+        const float2 ps = mul2(make_float2(dsum, dsum), a2);
+        const float2 Plo = make_float2(ex2f(pl.x), ex2f(pl.y));
+        const float2 Phi = make_float2(ex2f(ph.x), ex2f(ph.y));
+        float2 P = make_float2(ex2f(ps.x), ex2f(ps.y));
+        float2 S = fma2(Phi, Slo, Shi);
+        scan_pair_fwd<RL, 2>(P, S, j);
+        hout = fma2(P, hc, S);
+        float2 h;
+        h.x = __shfl_up_sync(0xffffffffu, hout.x, 2);
+        h.y = __shfl_up_sync(0xffffffffu, hout.y, 2);
+        if (j == 0) h = hc;
+        float2 h2 = fma2(Plo, h, Slo);  // state entering the second half
+#pragma unroll
+        for (int k = 0; k < H / 2; ++k) {
+          const float4 c = cq[k * RL];
+          const float4 c2 = cq[(k + H / 2) * RL];
+          h = fma2(a[2 * k], h, bb[2 * k]);
+          h2 = fma2(a[H + 2 * k], h2, bb[H + 2 * k]);
+          y[2 * k] = fmaf(c.y, h.y, fmaf(c.x, h.x, y[2 * k]));
+          y[H + 2 * k] = fmaf(c2.y, h2.y, fmaf(c2.x, h2.x, y[H + 2 * k]));
+          h = fma2(a[2 * k + 1], h, bb[2 * k + 1]);
+          h2 = fma2(a[H + 2 * k + 1], h2, bb[H + 2 * k + 1]);
+          y[2 * k + 1] = fmaf(c.w, h.y, fmaf(c.z, h.x, y[2 * k + 1]));
+          y[H + 2 * k + 1] = fmaf(c2.w, h2.y, fmaf(c2.z, h2.x, y[H + 2 * k + 1]));
+        }
+      }
+      if (j == RL - 1) *reinterpret_cast<float2*>(carry + ((cur ^ 1) * R + r) * kN + 2 * q) = hout;
+    }
+
+    if (zrow) {
+      float zz[KT];
+      decode_raw<Io, KT>(rz, zz);
+#pragma unroll
+      for (int i = 0; i < KT; ++i) y[i] *= zz[i] * sigmoid_f(zz[i]);
+    }
+    store_kt<Io, KT, true>(yrow, ts, L, valid, y);
+  }
+  cp_async_wait_all();
+  if (h_last) {
+    __syncthreads();
+    if (valid) h_last[row * kN + j] = carry[(cur * R + r) * kN + j];
+  }
+}
+
+template <typename Io, int W, int KT, bool kSplit = false>
+static cudaError_t launch_fwd_pair(const ScanArgs& a, void* y, float* h_last, cudaStream_t s) {
+  using Cfg = FwdPairCfg<Io, W, KT>;
+  auto kern = scan_fwd_pair_kernel<Io, W, KT, kSplit>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((a.Dch + Cfg::R - 1) / Cfg::R), (unsigned)a.Bsz);
+  kern<<<grid, W * 32, Cfg::smem, s>>>(a, static_cast<typename Io::T*>(y), h_last);
+  return cudaGetLastError();
+}
+
 template <typename Io, int W, bool kVec>
 static cudaError_t launch_fwd_t(const ScanArgs& a, void* y, float* h_last, cudaStream_t s) {
   constexpr int R = 2 * W;
@@ -133,14 +342,37 @@ static cudaError_t launch_fwd_t(const ScanArgs& a, void* y, float* h_last, cudaS
   return cudaGetLastError();
 }
 
+// Variant selector for experiments (0 = default).
+static int fwd_variant() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("SELSCAN_FWD_VARIANT");
+    v = e ? atoi(e) : 0;
+  }
+  return v;
+}
+
 cudaError_t launch_scan_fwd(const ScanArgs& a, void* y, float* h_last, cudaStream_t s) {
   constexpr int W = 8;
+  const int v = fwd_variant();
   if (a.dt == Dt::BF16) {
     const bool vec = (a.L % IoBf16::kVec) == 0;
+    if (vec && v == 0) return launch_fwd_pair<IoBf16, 4, 16>(a, y, h_last, s);
+    if (vec && v == 2) return launch_fwd_pair<IoBf16, 4, 8>(a, y, h_last, s);
+    if (vec && v == 3) return launch_fwd_pair<IoBf16, 8, 8>(a, y, h_last, s);
+    if (vec && v == 4) return launch_fwd_pair<IoBf16, 8, 16>(a, y, h_last, s);
+    if (vec && v == 5) return launch_fwd_pair<IoBf16, 4, 16, true>(a, y, h_last, s);
+    if (vec && v == 6) return launch_fwd_pair<IoBf16, 8, 8, true>(a, y, h_last, s);
     return vec ? launch_fwd_t<IoBf16, W, true>(a, y, h_last, s)
                : launch_fwd_t<IoBf16, W, false>(a, y, h_last, s);
   }
   const bool vec = (a.L % IoF32::kVec) == 0;
+  if (vec && v == 0) return launch_fwd_pair<IoF32, 4, 16>(a, y, h_last, s);
+  if (vec && v == 2) return launch_fwd_pair<IoF32, 4, 8>(a, y, h_last, s);
+  if (vec && v == 3) return launch_fwd_pair<IoF32, 8, 8>(a, y, h_last, s);
+  if (vec && v == 4) return launch_fwd_pair<IoF32, 8, 16>(a, y, h_last, s);
+  if (vec && v == 5) return launch_fwd_pair<IoF32, 4, 16, true>(a, y, h_last, s);
+  if (vec && v == 6) return launch_fwd_pair<IoF32, 8, 8, true>(a, y, h_last, s);
   return vec ? launch_fwd_t<IoF32, W, true>(a, y, h_last, s)
              : launch_fwd_t<IoF32, W, false>(a, y, h_last, s);
 }

@@ -74,7 +74,7 @@ def test_noalloc_matches_workspace_backward_on_consecutive_calls():
 
 def test_noalloc_refuses_problems_larger_than_its_buffer():
     limit = ss.lib().ss_scan_bwd_noalloc_max_scratch()
-    Bsz, Dch, L = 4, 1024, 2048
+    Bsz, Dch, L = 4, 1024, 4096
     assert ss.ss_scan_bwd_workspace_size(Bsz, Dch, L) > limit
     xd, dyd = _case("bf16", Bsz, Dch, L, 47)
     g = {k: v.fill_(3.0) for k, v in _alloc_grads(xd).items()}
