@@ -381,6 +381,47 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # GPU timing
 # ---------------------------------------------------------------------------
+def decode_step_measure(ss, dev, seed, steps=16):
+    """The one-token step on the decode workload (Bsz=256, Dch=5120, N=16,
+    bf16 tokens, float32 state): its state (84 MB) fits in L2, so L2 is
+    flushed (a 256 MiB write) before each timed step; the events bracket the
+    step kernel only.  Returns its time and HBM roofline."""
+    import torch
+    cfg = synth.config(4)
+    Bsz, Dch, N = cfg["Bsz"], cfg["Dch"], cfg["N"]
+    x = synth.make_inputs(dict(cfg, L=1), seed=seed)
+    tok = synth.step_inputs(cfg, 0, seed=seed)
+    bf = torch.bfloat16
+
+    def t(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).view(bf).to(dev)
+
+    u, dl, z, B, C = (t(tok[k]) for k in ("u", "delta", "z", "B", "C"))
+    A = torch.from_numpy(np.ascontiguousarray(x["A"], dtype=np.float32)).to(dev)
+    D = torch.from_numpy(np.ascontiguousarray(x["D"], dtype=np.float32)).to(dev)
+    bias = torch.from_numpy(np.ascontiguousarray(x["delta_bias"], dtype=np.float32)).to(dev)
+    h = torch.zeros((Bsz, Dch, N), device=dev, dtype=torch.float32)
+    y = torch.empty((Bsz, Dch), device=dev, dtype=bf)
+    flush = torch.empty(256 * 2 ** 20, device=dev, dtype=torch.uint8)
+    for _ in range(3):
+        ss.ss_step(h, u, dl, A, B, C, D, z, bias, True, out=y)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for e0, e1 in evs:
+        flush.fill_(1)
+        e0.record()
+        ss.ss_step(h, u, dl, A, B, C, D, z, bias, True, out=y)
+        e1.record()
+    torch.cuda.synchronize()
+    ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+    rows = Bsz * Dch
+    nbytes = rows * (2 * N * 4 + 4 * 2) + 2 * Bsz * N * 2  # h in/out, u/delta/z/y, B/C
+    hbm, _ = load_peaks()
+    ach = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"decode step Bsz={Bsz} Dch={Dch} N={N}, bf16 tokens, f32 state, "
+                        f"L2 flushed before each step", "ms": round(ms, 4),
+            "bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(ach / hbm, 4), "algorithmic_bytes": nbytes}
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -474,6 +515,8 @@ def run_ours(args):
     value = world * E / (ms * 1e-3) / 1e9
     fwd_gelem = E / (per_kernel["fwd"] * 1e-3) / 1e9
 
+    decode = decode_step_measure(ss, dev, seed) if rank == 0 else None
+
     # end to end through the public API with host buffers
     Ke = max(3, min(K, 10))
     outs = {"y": y, "yt": yt, **g}
@@ -517,6 +560,7 @@ def run_ours(args):
                          **({"frac": roofs[nm]["frac"], "bound": roofs[nm]["bound"]}
                             if nm in roofs else {})} for nm in names},
         "gpu_launches": K * LAUNCHES_PER_STEP,
+        "decode_step": decode,
         "e2e": {"value": round(world * E / (e2e_ms * 1e-3) / 1e9, 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 3)},

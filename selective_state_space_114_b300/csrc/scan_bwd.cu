@@ -256,8 +256,43 @@ struct MainSmem {
   static constexpr size_t acc = sizeof(float) * 2 * kN * CH;            // [dB,dC][n][CH]
   static constexpr size_t dA = sizeof(float) * R * kN * RL;             // [row][n][j]
   static constexpr size_t params = sizeof(float) * 4 * R * kN;          // A2, A, h_in, rho_in
-  static constexpr size_t total = pairs + slots + acc + dA + params;
+  // u, delta, z, dy segments of a pass, [buffer][tensor][vector][thread] 16-byte units
+  static constexpr size_t ins = 2ull * 4 * KT * sizeof(float) * (W * 32);  // sized for fp32
+  static constexpr size_t total = pairs + slots + acc + dA + params + ins;
 };
+
+// Copy the KT-step segments of u, delta, z, dy of one row into the lane's
+// slots of an input buffer (cp.async; zeros for an invalid row, for steps at
+// or past L and for an absent z).  Rows of 16-byte multiples only.
+template <typename Io, int KT, int NT>
+__device__ __forceinline__ void issue_row_inputs(const ScanArgs& p, const void* dy, int64_t row,
+                                                 bool valid, int64_t ts, int64_t L, uint4* buf,
+                                                 int tid) {
+  using T = typename Io::T;
+  constexpr int V = Io::kVec, VPL = KT / V;
+  const T* src[4] = {static_cast<const T*>(p.u) + row * L, static_cast<const T*>(p.delta) + row * L,
+                     p.z ? static_cast<const T*>(p.z) + row * L : nullptr,
+                     static_cast<const T*>(dy) + row * L};
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+      const int64_t t = ts + V * v;
+      const bool in = valid && src[w] != nullptr && t < L;
+      cp_async16(buf + (w * VPL + v) * NT + tid, in ? (const void*)(src[w] + t) : (const void*)src[0],
+                 in ? 16 : 0);
+    }
+  }
+}
+
+template <typename Io, int KT, int NT>
+__device__ __forceinline__ void read_row_input(const uint4* buf, int w, int tid, float (&v)[KT]) {
+  constexpr int V = Io::kVec, VPL = KT / V;
+  RawSeg<Io, KT> r;
+#pragma unroll
+  for (int k = 0; k < VPL; ++k) r.w[k] = buf[(w * VPL + k) * NT + tid];
+  decode_raw<Io, KT>(r, v);
+}
 
 // Four consecutive steps' values of the two states as two float4 stores.
 __device__ __forceinline__ void store_pair4(float* lo, float* hi, float2 v0, float2 v1, float2 v2,
@@ -405,6 +440,8 @@ __global__ void __launch_bounds__(W * 32)
   float* Ars = A2s + R * kN;
   float* Hs = Ars + R * kN;   // [row][n] state entering the chunk
   float* Rs = Hs + R * kN;    // [row][n] adjoint carry entering the chunk
+  uint4* ins = reinterpret_cast<uint4*>(sm + Sm::pairs + Sm::slots + Sm::acc + Sm::dA + Sm::params);
+  constexpr int kInsBuf = (int)(Sm::ins / 2 / sizeof(uint4));  // uint4 per buffer
   const float4* Bp = pairs;
   const float4* Cp = pairs + (kN / 2) * (KT / 2) * RL;
 
@@ -425,7 +462,13 @@ __global__ void __launch_bounds__(W * 32)
     static_assert(2 * kN * CH * sizeof(T) <= Sm::acc, "raw staging must fit");
     issue_raw_bc<Io, CH>(Bb, Cb, L, t0, raw, tid, NT);
     cp_async_commit();
-    cp_async_wait_all();
+    {
+      const int64_t d = g * kRowBlock + r;
+      issue_row_inputs<Io, KT, NT>(p, o.dy, b * p.Dch + (d < p.Dch ? d : 0), d < p.Dch,
+                                   t0 + KT * j, L, ins, tid);
+    }
+    cp_async_commit();
+    cp_async_wait_one();  // B / C landed (the inputs may still be in flight)
     __syncthreads();
     raw_to_pairs<Io, CH, KT, RL>(raw, pairs, tid, NT);
     __syncthreads();
@@ -473,15 +516,32 @@ __global__ void __launch_bounds__(W * 32)
     const float* hin_row = Hs + r * kN;
     const float* rin_row = Rs + r * kN;
 
+    const uint4* inb = ins + (pass & 1) * kInsBuf;  // this pass's inputs (16-byte rows)
+    if (kVec) {
+      // next pass's inputs go in flight now; this pass's have landed after the wait
+      const int64_t dn = d + R;
+      if (pass + 1 < kPasses && d0 + R < p.Dch)
+        issue_row_inputs<Io, KT, NT>(p, o.dy, b * p.Dch + (dn < p.Dch ? dn : 0), dn < p.Dch, ts,
+                                     L, ins + ((pass + 1) & 1) * kInsBuf, tid);
+      cp_async_commit();
+      cp_async_wait_one();
+    }
     float dl[KT];
     float2 du2[KT], yh2[KT], yacc2[KT], s12[KT], s22[KT];
     float dD_acc = 0.f, dsum = 0.f;
     {
       float uu[KT], zz[KT], gg[KT];
-      load_kt<Io, KT, kVec>(urow, ts, L, valid, uu);
-      load_kt<Io, KT, kVec>(drow, ts, L, valid, dl);
-      load_kt<Io, KT, kVec>(zrow, ts, L, valid && zrow != nullptr, zz);
-      load_kt<Io, KT, kVec>(grow, ts, L, valid, gg);
+      if (kVec) {
+        read_row_input<Io, KT, NT>(inb, 0, tid, uu);
+        read_row_input<Io, KT, NT>(inb, 1, tid, dl);
+        read_row_input<Io, KT, NT>(inb, 2, tid, zz);
+        read_row_input<Io, KT, NT>(inb, 3, tid, gg);
+      } else {
+        load_kt<Io, KT, kVec>(urow, ts, L, valid, uu);
+        load_kt<Io, KT, kVec>(drow, ts, L, valid, dl);
+        load_kt<Io, KT, kVec>(zrow, ts, L, valid && zrow != nullptr, zz);
+        load_kt<Io, KT, kVec>(grow, ts, L, valid, gg);
+      }
 #pragma unroll
       for (int i = 0; i < KT; ++i) {
         const bool in = valid && ts + i < L;
@@ -509,26 +569,36 @@ __global__ void __launch_bounds__(W * 32)
       __syncthreads();
       if (tid < 2 * 2 * CH / 4) {
         const float* base = slots + (size_t)(q & 1) * R * SR + sum_e;
-        float4 sacc = *reinterpret_cast<const float4*>(base);
+        float4 v = *reinterpret_cast<const float4*>(base);
+        float2 lo = make_float2(v.x, v.y), hi = make_float2(v.z, v.w);
 #pragma unroll
         for (int rr = 1; rr < R; ++rr) {
-          const float4 v = *reinterpret_cast<const float4*>(base + (size_t)rr * SR);
-          sacc.x += v.x; sacc.y += v.y; sacc.z += v.z; sacc.w += v.w;
+          v = *reinterpret_cast<const float4*>(base + (size_t)rr * SR);
+          lo = add2(lo, make_float2(v.x, v.y));
+          hi = add2(hi, make_float2(v.z, v.w));
         }
         float4* ap = reinterpret_cast<float4*>(acc + ((size_t)sum_wh * kN + 2 * q + sum_nl) * CH + sum_t);
-        float4 av = *ap;
-        av.x += sacc.x; av.y += sacc.y; av.z += sacc.z; av.w += sacc.w;
-        *ap = av;
+        v = *ap;
+        lo = add2(lo, make_float2(v.x, v.y));
+        hi = add2(hi, make_float2(v.z, v.w));
+        *ap = make_float4(lo.x, lo.y, hi.x, hi.y);
       }
     }
 
     // per-time-step outputs
     {
       float uu[KT], dr[KT], zz[KT], gg[KT], o1[KT], o2[KT], o3[KT];
-      load_kt<Io, KT, kVec>(urow, ts, L, valid, uu);
-      load_kt<Io, KT, kVec>(drow, ts, L, valid, dr);
-      load_kt<Io, KT, kVec>(zrow, ts, L, valid && zrow != nullptr, zz);
-      load_kt<Io, KT, kVec>(grow, ts, L, valid, gg);
+      if (kVec) {
+        read_row_input<Io, KT, NT>(inb, 0, tid, uu);
+        read_row_input<Io, KT, NT>(inb, 1, tid, dr);
+        read_row_input<Io, KT, NT>(inb, 2, tid, zz);
+        read_row_input<Io, KT, NT>(inb, 3, tid, gg);
+      } else {
+        load_kt<Io, KT, kVec>(urow, ts, L, valid, uu);
+        load_kt<Io, KT, kVec>(drow, ts, L, valid, dr);
+        load_kt<Io, KT, kVec>(zrow, ts, L, valid && zrow != nullptr, zz);
+        load_kt<Io, KT, kVec>(grow, ts, L, valid, gg);
+      }
       float dbias_acc = 0.f;
 #pragma unroll
       for (int i = 0; i < KT; ++i) {

@@ -184,3 +184,11 @@ def test_empty_backward_zero_gradients():
     torch.cuda.synchronize()
     assert torch.all(out["dA"] == 0) and torch.all(out["dD"] == 0)
     assert torch.all(out["ddelta_bias"] == 0)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_softplus_extremes_backward(dtype):
+    x = make_case(dtype, 2, 20, 390, seed=33, with_dy=True)
+    d = synth.widen(x["delta"]) * 20.0
+    x["delta"] = synth.to_bf16(d.astype(np.float32)) if dtype == "bf16" else d.astype(np.float32)
+    compare(x, dtype, what=f"{dtype} softplus extremes")

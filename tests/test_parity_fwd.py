@@ -151,3 +151,13 @@ def test_config3_full_size_sampled_rows():
     rng = np.random.default_rng(3)
     rows = [(0, 0), (0, 5119)] + [(0, int(rng.integers(5120))) for _ in range(6)]
     _full_config_sampled(3, rows)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_softplus_extremes(dtype):
+    """delta_raw spread over about +-60: both branches of the GPU's log1p
+    (series below e^-|x| = 1/32, log2 above) and the saturated ends."""
+    x = make_case(dtype, 2, 24, 520, seed=31)
+    d = synth.widen(x["delta"]) * 20.0
+    x["delta"] = synth.to_bf16(d.astype(np.float32)) if dtype == "bf16" else d.astype(np.float32)
+    compare(x, dtype, what=f"{dtype} softplus extremes")
