@@ -384,8 +384,9 @@ def run_reference(args):
 def decode_step_measure(ss, dev, seed, steps=16):
     """The one-token step on the decode workload (Bsz=256, Dch=5120, N=16,
     bf16 tokens, float32 state): its state (84 MB) fits in L2, so L2 is
-    flushed (a 256 MiB write) before each timed step; the events bracket the
-    step kernel only.  Returns its time and HBM roofline."""
+    flushed before each timed step by reading a 256 MiB buffer (a read leaves
+    no dirty lines to be written back during the step); the events bracket
+    the step kernel only.  Returns its time and HBM roofline."""
     import torch
     cfg = synth.config(4)
     Bsz, Dch, N = cfg["Bsz"], cfg["Dch"], cfg["N"]
@@ -402,13 +403,14 @@ def decode_step_measure(ss, dev, seed, steps=16):
     bias = torch.from_numpy(np.ascontiguousarray(x["delta_bias"], dtype=np.float32)).to(dev)
     h = torch.zeros((Bsz, Dch, N), device=dev, dtype=torch.float32)
     y = torch.empty((Bsz, Dch), device=dev, dtype=bf)
-    flush = torch.empty(256 * 2 ** 20, device=dev, dtype=torch.uint8)
+    flush = torch.ones(64 * 2 ** 20, device=dev, dtype=torch.float32)  # 256 MiB
+    sink = torch.empty((), device=dev, dtype=torch.float32)
     for _ in range(3):
         ss.ss_step(h, u, dl, A, B, C, D, z, bias, True, out=y)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
     for e0, e1 in evs:
-        flush.fill_(1)
+        torch.sum(flush, dim=0, out=sink)
         e0.record()
         ss.ss_step(h, u, dl, A, B, C, D, z, bias, True, out=y)
         e1.record()

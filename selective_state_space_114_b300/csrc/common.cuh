@@ -374,6 +374,11 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, int
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// Wait until at most N committed groups (the newest ones) are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_depth() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 // Wait until at most one committed group (the newest) is still in flight.
 __device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 

@@ -47,6 +47,7 @@ constexpr int kRLb = 16;                   // lanes per row
 constexpr int kBwdChunk = kKTb * kRLb;     // 128 steps per chunk
 constexpr int kRowBlock = 128;             // rows per CTA (main kernel)
 constexpr int kSumThreads = 128;           // rows per CTA (summary kernel)
+constexpr int kSumDepth = 3;               // input blocks in flight (summary kernel)
 
 struct WsLayout {
   size_t sumS, sumQ, dsum, pbc, pa, pd, pbias, total;
@@ -87,9 +88,10 @@ __global__ void __launch_bounds__(kSumThreads)
                        float* __restrict__ sumQ, float* __restrict__ dsum_out) {
   using T = typename Io::T;
   constexpr int CH = kBwdChunk;
-  __shared__ float4 sB4[CH * kN / 4], sC4[CH * kN / 4];  // [t][n]
-  float* sB = reinterpret_cast<float*>(sB4);
-  float* sC = reinterpret_cast<float*>(sC4);
+  extern __shared__ float4 smem4[];
+  float* sB = reinterpret_cast<float*>(smem4);  // [t][n]
+  float* sC = sB + CH * kN;                      // [t][n]
+  uint4* ring = reinterpret_cast<uint4*>(sC + CH * kN);  // input ring (16-byte rows only)
   const int tid = threadIdx.x;
   const int64_t c = blockIdx.x / nrb;
   const int64_t rb = blockIdx.x - c * nrb;
@@ -136,30 +138,52 @@ __global__ void __launch_bounds__(kSumThreads)
     cp[q] = make_float2(1.f, 1.f);
   }
   float dsum = 0.f;
-  // 8-step blocks; with 16-byte rows the next block's inputs are loaded while
-  // the current one is processed
-  RawSeg<Io, 8> nu, nd, nz, ng;
+  // 8-step blocks.  With 16-byte rows each thread keeps the inputs of the next
+  // kSumDepth - 1 blocks in flight (cp.async into a per-thread ring in shared
+  // memory, [slot][tensor][vector][thread] 16-byte units).
+  constexpr int VPB = 8 / Io::kVec;  // 16-byte vectors per tensor per block
+  auto issue_block = [&](int tb) {
+    uint4* slot = ring + ((tb / 8) % kSumDepth) * 4 * VPB * kSumThreads;
+    const T* src[4] = {urow, drow, zrow, grow};
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+#pragma unroll
+      for (int v = 0; v < VPB; ++v) {
+        const int64_t t = t0 + tb + Io::kVec * v;
+        const bool in = tb < CH && src[w] != nullptr && t < L;
+        cp_async16(slot + (w * VPB + v) * kSumThreads + tid,
+                   in ? (const void*)(src[w] + t) : (const void*)urow, in ? 16 : 0);
+      }
+  };
   if (kVec) {
-    load_raw<Io, 8>(urow, t0, L, true, nu);
-    load_raw<Io, 8>(drow, t0, L, true, nd);
-    load_raw<Io, 8>(zrow, t0, L, zrow != nullptr, nz);
-    load_raw<Io, 8>(grow, t0, L, true, ng);
+#pragma unroll
+    for (int k = 0; k < kSumDepth - 1; ++k) {
+      issue_block(8 * k);
+      cp_async_commit();
+    }
   }
 #pragma unroll 1
   for (int tb = 0; tb < CH; tb += 8) {
     const int64_t t = t0 + tb;
     float uu[8], dd[8], zz[8], gg[8];
     if (kVec) {
-      decode_raw<Io, 8>(nu, uu);
-      decode_raw<Io, 8>(nd, dd);
-      decode_raw<Io, 8>(nz, zz);
-      decode_raw<Io, 8>(ng, gg);
-      if (tb + 8 < CH) {
-        load_raw<Io, 8>(urow, t + 8, L, true, nu);
-        load_raw<Io, 8>(drow, t + 8, L, true, nd);
-        load_raw<Io, 8>(zrow, t + 8, L, zrow != nullptr, nz);
-        load_raw<Io, 8>(grow, t + 8, L, true, ng);
-      }
+      issue_block(tb + 8 * (kSumDepth - 1));
+      cp_async_commit();
+      cp_async_wait_depth<kSumDepth - 1>();  // block tb has landed
+      const uint4* slot = ring + ((tb / 8) % kSumDepth) * 4 * VPB * kSumThreads + tid;
+      RawSeg<Io, 8> r;
+#pragma unroll
+      for (int v = 0; v < VPB; ++v) r.w[v] = slot[(0 * VPB + v) * kSumThreads];
+      decode_raw<Io, 8>(r, uu);
+#pragma unroll
+      for (int v = 0; v < VPB; ++v) r.w[v] = slot[(1 * VPB + v) * kSumThreads];
+      decode_raw<Io, 8>(r, dd);
+#pragma unroll
+      for (int v = 0; v < VPB; ++v) r.w[v] = slot[(2 * VPB + v) * kSumThreads];
+      decode_raw<Io, 8>(r, zz);
+#pragma unroll
+      for (int v = 0; v < VPB; ++v) r.w[v] = slot[(3 * VPB + v) * kSumThreads];
+      decode_raw<Io, 8>(r, gg);
     } else {
       load_kt<Io, 8, kVec>(urow, t, L, true, uu);
       load_kt<Io, 8, kVec>(drow, t, L, true, dd);
@@ -246,18 +270,18 @@ __global__ void bwd_carry_kernel(const float* __restrict__ A, int64_t Bsz, int64
 // writes its dB / dC terms to its own slot; after a barrier the 256 threads
 // sum the 16 rows' slots into the block accumulator.
 // ---------------------------------------------------------------------------
-template <int W>
+template <int W, typename T, int kSlotBufs>
 struct MainSmem {
   static constexpr int KT = kKTb, RL = kRLb, CH = kBwdChunk, R = 2 * W;
   static constexpr size_t pairs = sizeof(float4) * 2 * (kN / 2) * (KT / 2) * RL;  // B, C
   static constexpr size_t slot_row = 2 * 2 * CH + 4;  // [dB,dC][2][CH] floats, padded so the
                                                       // two rows of a warp use other banks
-  static constexpr size_t slots = sizeof(float) * 2 * R * slot_row;     // [parity][row]
+  static constexpr size_t slots = sizeof(float) * kSlotBufs * R * slot_row;  // [buffer][row]
   static constexpr size_t acc = sizeof(float) * 2 * kN * CH;            // [dB,dC][n][CH]
   static constexpr size_t dA = sizeof(float) * R * kN * RL;             // [row][n][j]
   static constexpr size_t params = sizeof(float) * 4 * R * kN;          // A2, A, h_in, rho_in
   // u, delta, z, dy segments of a pass, [buffer][tensor][vector][thread] 16-byte units
-  static constexpr size_t ins = 2ull * 4 * KT * sizeof(float) * (W * 32);  // sized for fp32
+  static constexpr size_t ins = 2ull * 4 * KT * sizeof(T) * (W * 32);
   static constexpr size_t total = pairs + slots + acc + dA + params + ins;
 };
 
@@ -420,13 +444,13 @@ __device__ __forceinline__ void bwd_state_pair(
 
 }
 
-template <typename Io, bool kVec, int W>
-__global__ void __launch_bounds__(W * 32)
+template <typename Io, bool kVec, int W, int kMinBlocks, int kSlotBufs>
+__global__ void __launch_bounds__(W * 32, kMinBlocks)
     bwd_main_kernel(ScanArgs p, BwdOut o, int64_t nrb, const float* __restrict__ Hin,
                     const float* __restrict__ Rin, float* __restrict__ pBC,
                     float* __restrict__ pA, float* __restrict__ pD, float* __restrict__ pbias) {
   using T = typename Io::T;
-  using Sm = MainSmem<W>;
+  using Sm = MainSmem<W, T, kSlotBufs>;
   constexpr int KT = kKTb, RL = kRLb, CH = kBwdChunk, R = 2 * W, NT = W * 32;
   constexpr int kPasses = kRowBlock / R;
   constexpr int SR = (int)Sm::slot_row;
@@ -560,7 +584,8 @@ __global__ void __launch_bounds__(W * 32)
 
 #pragma unroll 1
     for (int q = 0; q < kN / 2; ++q) {
-      float* slot = my_slot0 + (size_t)(q & 1) * R * SR;
+      const int sb = kSlotBufs == 2 ? (q & 1) : 0;
+      float* slot = my_slot0 + (size_t)sb * R * SR;
       bwd_state_pair<KT, RL, CH>(q, j, r, valid, A2s, Ars, hin_row, rin_row, Bp, Cp, dl, du2, yh2,
                                  dsum, yacc2, s12, s22, slot, slot + 2 * CH,
                                  dAs + (r * kN + 2 * q) * RL + j);
@@ -568,7 +593,7 @@ __global__ void __launch_bounds__(W * 32)
       // dB / dC of this state pair: sum the rows' slots into the accumulator
       __syncthreads();
       if (tid < 2 * 2 * CH / 4) {
-        const float* base = slots + (size_t)(q & 1) * R * SR + sum_e;
+        const float* base = slots + (size_t)sb * R * SR + sum_e;
         float4 v = *reinterpret_cast<const float4*>(base);
         float2 lo = make_float2(v.x, v.y), hi = make_float2(v.z, v.w);
 #pragma unroll
@@ -583,6 +608,7 @@ __global__ void __launch_bounds__(W * 32)
         hi = add2(hi, make_float2(v.z, v.w));
         *ap = make_float4(lo.x, lo.y, hi.x, hi.y);
       }
+      if (kSlotBufs == 1) __syncthreads();  // the single slot buffer is free again
     }
 
     // per-time-step outputs
@@ -669,27 +695,53 @@ __global__ void bwd_reduce_bc_kernel(const float* __restrict__ pBC, int64_t nrb,
   (wh ? dC : dB)[e] = acc;
 }
 
-__global__ void bwd_reduce_param_kernel(const float* __restrict__ pA, const float* __restrict__ pD,
-                                        const float* __restrict__ pbias, int64_t Bsz, int64_t Dch,
-                                        int64_t nch, float* __restrict__ dA, float* __restrict__ dD,
-                                        float* __restrict__ dbias) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < Dch * kN) {
-    const int64_t d = i / kN, n = i % kN;
-    float acc = 0.f;
-    for (int64_t b = 0; b < Bsz; ++b)
-      for (int64_t c = 0; c < nch; ++c) acc += pA[((b * Dch + d) * nch + c) * kN + n];
-    dA[i] = acc;
-  }
-  if (i < Dch) {
-    float a1 = 0.f, a2 = 0.f;
-    for (int64_t b = 0; b < Bsz; ++b)
+// One CTA per channel d.  Thread (g, n), g = 0..7, sums the chunk partials of
+// batches g, g + 8, g + 16, ... (batch, then chunk order); the eight group
+// sums are then added in order of g.  Fixed order: bitwise reproducible.
+constexpr int kParamGroups = 8;
+__global__ void __launch_bounds__(kParamGroups * kN)
+    bwd_reduce_param_kernel(const float* __restrict__ pA, const float* __restrict__ pD,
+                            const float* __restrict__ pbias, int64_t Bsz, int64_t Dch,
+                            int64_t nch, float* __restrict__ dA, float* __restrict__ dD,
+                            float* __restrict__ dbias) {
+  __shared__ float sA[kParamGroups * kN], sD[kParamGroups], sB[kParamGroups];
+  const int64_t d = blockIdx.x;
+  const int tid = threadIdx.x, n = tid % kN, gq = tid / kN;
+  float acc = 0.f, a1 = 0.f, a2 = 0.f;
+  for (int64_t b = gq; b < Bsz; b += kParamGroups) {
+    const int64_t rc0 = (b * Dch + d) * nch;
+    const float* src = pA + rc0 * kN + n;
+#pragma unroll 8
+    for (int64_t c = 0; c < nch; ++c) acc += src[c * kN];
+    if (n == 0) {
+#pragma unroll 8
       for (int64_t c = 0; c < nch; ++c) {
-        a1 += pD[(b * Dch + i) * nch + c];
-        a2 += pbias[(b * Dch + i) * nch + c];
+        a1 += pD[rc0 + c];
+        a2 += pbias[rc0 + c];
       }
-    if (dD) dD[i] = a1;
-    if (dbias) dbias[i] = a2;
+    }
+  }
+  sA[tid] = acc;
+  if (n == 0) {
+    sD[gq] = a1;
+    sB[gq] = a2;
+  }
+  __syncthreads();
+  if (tid < kN) {
+    float t = 0.f;
+#pragma unroll
+    for (int g = 0; g < kParamGroups; ++g) t += sA[g * kN + tid];
+    dA[d * kN + tid] = t;
+  }
+  if (tid == 0) {
+    float t1 = 0.f, t2 = 0.f;
+#pragma unroll
+    for (int g = 0; g < kParamGroups; ++g) {
+      t1 += sD[g];
+      t2 += sB[g];
+    }
+    if (dD) dD[d] = t1;
+    if (dbias) dbias[d] = t2;
   }
 }
 
@@ -703,12 +755,12 @@ int bwd_variant() {
   return v;
 }
 
-template <typename Io, bool kVec, int W>
+template <typename Io, bool kVec, int W, int kMinBlocks, int kSlotBufs>
 cudaError_t launch_main(const ScanArgs& a, const BwdOut& o, const WsLayout& w, float* sumS,
                         float* sumQ, float* pBC, float* pA, float* pD, float* pbias,
                         cudaStream_t s) {
-  using Sm = MainSmem<W>;
-  auto kern = bwd_main_kernel<Io, kVec, W>;
+  using Sm = MainSmem<W, typename Io::T, kSlotBufs>;
+  auto kern = bwd_main_kernel<Io, kVec, W, kMinBlocks, kSlotBufs>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sm::total);
   if (e != cudaSuccess) return e;
@@ -732,7 +784,12 @@ cudaError_t launch_bwd_t(int phase, const ScanArgs& a, const BwdOut& o, void* ws
   if (phase == 0) {
     const int64_t nrb = (a.Dch + kSumThreads - 1) / kSumThreads;
     dim3 grid((unsigned)(nrb * w.nchunks), (unsigned)a.Bsz);
-    bwd_summary_kernel<Io, kVec><<<grid, kSumThreads, 0, s>>>(a, o, nrb, sumS, sumQ, dsum);
+    const size_t smem = sizeof(float) * 2 * kBwdChunk * kN +
+                        (kVec ? sizeof(uint4) * kSumDepth * 4 * (8 / Io::kVec) * kSumThreads : 0);
+    auto kern = bwd_summary_kernel<Io, kVec>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kSumThreads, smem, s>>>(a, o, nrb, sumS, sumQ, dsum);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t n = a.Bsz * a.Dch * kN;
     bwd_carry_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a.A, a.Bsz, a.Dch, w.nchunks,
@@ -740,15 +797,18 @@ cudaError_t launch_bwd_t(int phase, const ScanArgs& a, const BwdOut& o, void* ws
     return cudaGetLastError();
   }
   if (phase == 1) {
-    return bwd_variant() == 1 ? launch_main<Io, kVec, 8>(a, o, w, sumS, sumQ, pBC, pA, pD, pbias, s)
-                              : launch_main<Io, kVec, 4>(a, o, w, sumS, sumQ, pBC, pA, pD, pbias, s);
+    switch (bwd_variant()) {
+      case 1: return launch_main<Io, kVec, 8, 1, 2>(a, o, w, sumS, sumQ, pBC, pA, pD, pbias, s);
+      case 2: return launch_main<Io, kVec, 4, 2, 2>(a, o, w, sumS, sumQ, pBC, pA, pD, pbias, s);
+      case 3: return launch_main<Io, kVec, 4, 3, 2>(a, o, w, sumS, sumQ, pBC, pA, pD, pbias, s);
+      default: return launch_main<Io, kVec, 4, 3, 1>(a, o, w, sumS, sumQ, pBC, pA, pD, pbias, s);
+    }
   }
   const int64_t n = 2 * a.Bsz * kN * a.L;
   bwd_reduce_bc_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(pBC, w.blocks, a.Bsz, a.L,
                                                                      o.dB, o.dC);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const int64_t m = a.Dch * kN;
-  bwd_reduce_param_kernel<<<(unsigned)((m + 255) / 256), 256, 0, s>>>(
+  bwd_reduce_param_kernel<<<(unsigned)a.Dch, kParamGroups * kN, 0, s>>>(
       pA, pD, pbias, a.Bsz, a.Dch, w.nchunks, o.dA, o.dD, o.ddelta_bias);
   return cudaGetLastError();
 }
