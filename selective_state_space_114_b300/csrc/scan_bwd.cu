@@ -274,10 +274,10 @@ template <int W, typename T, int kSlotBufs>
 struct MainSmem {
   static constexpr int KT = kKTb, RL = kRLb, CH = kBwdChunk, R = 2 * W;
   static constexpr size_t pairs = sizeof(float4) * 2 * (kN / 2) * (KT / 2) * RL;  // B, C
-  static constexpr size_t slot_row = 2 * 2 * CH + 4;  // [dB,dC][2][CH] floats, padded so the
-                                                      // two rows of a warp use other banks
+  static constexpr size_t slot_row = 2 * CH * 2 + 4;  // [dB,dC][CH][2 states] floats, padded
+                                                      // so the two rows of a warp use other banks
   static constexpr size_t slots = sizeof(float) * kSlotBufs * R * slot_row;  // [buffer][row]
-  static constexpr size_t acc = sizeof(float) * 2 * kN * CH;            // [dB,dC][n][CH]
+  static constexpr size_t acc = sizeof(float) * 2 * kN * CH;            // [dB,dC][q][CH][2]
   static constexpr size_t dA = sizeof(float) * R * kN * RL;             // [row][n][j]
   static constexpr size_t params = sizeof(float) * 4 * R * kN;          // A2, A, h_in, rho_in
   // u, delta, z, dy segments of a pass, [buffer][tensor][vector][thread] 16-byte units
@@ -318,12 +318,20 @@ __device__ __forceinline__ void read_row_input(const uint4* buf, int w, int tid,
   decode_raw<Io, KT>(r, v);
 }
 
-// Four consecutive steps' values of the two states as two float4 stores.
-__device__ __forceinline__ void store_pair4(float* lo, float* hi, float2 v0, float2 v1, float2 v2,
-                                            float2 v3) {
-  *reinterpret_cast<float4*>(lo) = make_float4(v0.x, v1.x, v2.x, v3.x);
-  *reinterpret_cast<float4*>(hi) = make_float4(v0.y, v1.y, v2.y, v3.y);
+// KT steps of a state pair, stored as [step][state]: two steps per float4.
+// The lane's KT / 2 float4 are rotated by sw (slot_swizzle) so that the eight
+// lanes of a quarter-warp (four segments j, two rows) hit eight different
+// 16-byte bank groups.
+template <int KT>
+__device__ __forceinline__ void store_steps(float* dst, const float2 (&v)[KT], int sw) {
+#pragma unroll
+  for (int i = 0; i < KT; i += 2) {
+    const int k = ((i >> 1) + sw) & (KT / 2 - 1);
+    *reinterpret_cast<float4*>(dst + 4 * k) = make_float4(v[i].x, v[i].y, v[i + 1].x, v[i + 1].y);
+  }
 }
+
+__device__ __forceinline__ int slot_swizzle(int j) { return 2 * ((j >> 1) & 1); }
 
 // One state pair q of one row: forward fold / scan / replay, reverse fold /
 // scan / replay and the products.  Accumulates the per-step sums over states
@@ -416,8 +424,7 @@ __device__ __forceinline__ void bwd_state_pair(
       yacc2[2 * k + 1] = fma2(c1, h, yacc2[2 * k + 1]);
       bb[2 * k + 1] = mul2(yh2[2 * k + 1], h);
     }
-    store_pair4(dC_lo, dC_lo + CH, bb[0], bb[1], bb[2], bb[3]);
-    store_pair4(dC_lo + 4, dC_lo + CH + 4, bb[4], bb[5], bb[6], bb[7]);
+    store_steps<KT>(dC_lo, bb, slot_swizzle(j));
 
     // reverse replay: lam_t and the products
     float2 lam = add2(mu[KT - 1], rin);
@@ -437,8 +444,7 @@ __device__ __forceinline__ void bwd_state_pair(
         dA2 = fma2(make_float2(dl[i], dl[i]), lq, dA2);
       }
     }
-    store_pair4(dB_lo, dB_lo + CH, bb[0], bb[1], bb[2], bb[3]);
-    store_pair4(dB_lo + 4, dB_lo + CH + 4, bb[4], bb[5], bb[6], bb[7]);
+    store_steps<KT>(dB_lo, bb, slot_swizzle(j));
     dA_lo[0] = dA2.x;   // state 2q
   dA_lo[RL] = dA2.y;  // state 2q + 1
 
@@ -502,12 +508,16 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks)
   for (int i = tid; i < 2 * kN * CH; i += NT) acc[i] = 0.f;
 
   const int64_t ts = t0 + KT * j;
-  float* my_slot0 = slots + (size_t)r * SR + KT * j;  // + parity * R * SR
+  float* my_slot0 = slots + (size_t)r * SR + 2 * KT * j;  // + buffer * R * SR
   // cross-row sum assignment: thread -> four consecutive floats of [dB,dC][2][CH]
   const int sum_e = 4 * tid;                      // element of the row slot
   const int sum_wh = sum_e / (2 * CH);            // 0: dB, 1: dC
-  const int sum_nl = (sum_e / CH) & 1;            // state within the pair
-  const int sum_t = sum_e % CH;
+  const int sum_st = sum_e % (2 * CH);            // (step, state) within the tensor
+  // where store_steps put that float4: segment js, rotated position
+  const int sum_js = (sum_st / 4) / (KT / 2);
+  const int sum_phys = sum_wh * 2 * CH +
+                       4 * (sum_js * (KT / 2) + (((sum_st / 4) % (KT / 2) + slot_swizzle(sum_js)) & (KT / 2 - 1)));
+  static_assert(KT == 8, "the slot swizzle assumes four float4 per lane segment");
   static_assert(4 * NT >= 2 * 2 * CH, "one float4 of the row slot per summing thread");
 
 #pragma unroll 1
@@ -593,7 +603,7 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks)
       // dB / dC of this state pair: sum the rows' slots into the accumulator
       __syncthreads();
       if (tid < 2 * 2 * CH / 4) {
-        const float* base = slots + (size_t)sb * R * SR + sum_e;
+        const float* base = slots + (size_t)sb * R * SR + sum_phys;
         float4 v = *reinterpret_cast<const float4*>(base);
         float2 lo = make_float2(v.x, v.y), hi = make_float2(v.z, v.w);
 #pragma unroll
@@ -602,7 +612,7 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks)
           lo = add2(lo, make_float2(v.x, v.y));
           hi = add2(hi, make_float2(v.z, v.w));
         }
-        float4* ap = reinterpret_cast<float4*>(acc + ((size_t)sum_wh * kN + 2 * q + sum_nl) * CH + sum_t);
+        float4* ap = reinterpret_cast<float4*>(acc + ((size_t)sum_wh * (kN / 2) + q) * 2 * CH + sum_st);
         v = *ap;
         lo = add2(lo, make_float2(v.x, v.y));
         hi = add2(hi, make_float2(v.z, v.w));
@@ -676,7 +686,8 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks)
   float* out = pBC + ((size_t)(b * nrb + g) * 2) * kN * L;
   for (int i = tid; i < 2 * kN * CH; i += NT) {
     const int whn = i / CH, tt = i % CH;  // (wh * kN + n, t)
-    if (t0 + tt < L) out[(size_t)whn * L + t0 + tt] = acc[i];
+    const int wh = whn / kN, n = whn % kN;
+    if (t0 + tt < L) out[(size_t)whn * L + t0 + tt] = acc[((wh * (kN / 2) + n / 2) * CH + tt) * 2 + (n & 1)];
   }
 }
 
