@@ -36,8 +36,6 @@
 #include "common.cuh"
 #include "launch.h"
 
-#include <stdlib.h>
-
 namespace selscan {
 
 namespace {
@@ -756,16 +754,6 @@ __global__ void __launch_bounds__(kParamGroups * kN)
   }
 }
 
-// Variant selector for experiments (0 = default).
-int bwd_variant() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = getenv("SELSCAN_BWD_VARIANT");
-    v = e ? atoi(e) : 0;
-  }
-  return v;
-}
-
 template <typename Io, bool kVec, int W, int kMinBlocks, int kSlotBufs>
 cudaError_t launch_main(const ScanArgs& a, const BwdOut& o, const WsLayout& w, float* sumS,
                         float* sumQ, float* pBC, float* pA, float* pD, float* pbias,
@@ -808,12 +796,10 @@ cudaError_t launch_bwd_t(int phase, const ScanArgs& a, const BwdOut& o, void* ws
     return cudaGetLastError();
   }
   if (phase == 1) {
-    switch (bwd_variant()) {
-      case 1: return launch_main<Io, kVec, 8, 1, 2>(a, o, w, sumS, sumQ, pBC, pA, pD, pbias, s);
-      case 2: return launch_main<Io, kVec, 4, 2, 2>(a, o, w, sumS, sumQ, pBC, pA, pD, pbias, s);
-      case 3: return launch_main<Io, kVec, 4, 3, 2>(a, o, w, sumS, sumQ, pBC, pA, pD, pbias, s);
-      default: return launch_main<Io, kVec, 4, 3, 1>(a, o, w, sumS, sumQ, pBC, pA, pD, pbias, s);
-    }
+    // 4 warps per CTA, registers capped for three CTAs per SM (167 used, no
+    // spills), one dB/dC slot buffer so that three CTAs also fit in shared
+    // memory: 12 warps per SM (measured fastest of 8/12 warps, 1/2 buffers)
+    return launch_main<Io, kVec, 4, 3, 1>(a, o, w, sumS, sumQ, pBC, pA, pD, pbias, s);
   }
   const int64_t n = 2 * a.Bsz * kN * a.L;
   bwd_reduce_bc_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(pBC, w.blocks, a.Bsz, a.L,

@@ -7,16 +7,17 @@
 // sequential loop of the "PyTorch 한 파일에서의 Mamba 구현" thread
 // (news.hada.io, topic 12448), evaluated here as a chunked parallel scan.
 //
-// Grid: x = channel groups of R = 2W rows, y = batch.  Each warp holds two
-// rows; lanes of a half-warp split the current 256-step chunk into 16-step
-// segments (see common.cuh).  The CTA stages B and C of its batch for the
-// chunk once in shared memory (as float) and every row reuses them.  The
-// state crossing chunk boundaries lives in shared memory (carry), so a CTA
-// walks the whole sequence with no second pass.
+// Two kernels.  scan_fwd_pair_kernel (below) serves rows whose byte length
+// is a multiple of 16; scan_fwd_kernel, the element-wise version of the same
+// scheme, serves any other L.  Common scheme -- grid: x = channel groups of
+// R = 2W rows, y = batch.  Each warp holds two rows; the lanes of a row
+// split the current chunk into consecutive segments (see common.cuh).  The
+// CTA stages B and C of its batch for the chunk once in shared memory (as
+// float) and every row reuses them.  The state crossing chunk boundaries
+// lives in shared memory (carry), so a CTA walks the whole sequence with no
+// second pass.
 #include "common.cuh"
 #include "launch.h"
-
-#include <stdlib.h>
 
 namespace selscan {
 
@@ -135,7 +136,7 @@ __global__ void __launch_bounds__(W * 32)
 // and u / delta of the next chunk are prefetched into registers while the
 // current chunk is scanned.
 // ---------------------------------------------------------------------------
-template <typename Io, int W, int KT, bool kSplit = false>
+template <typename Io, int W, int KT>
 struct FwdPairCfg {
   static constexpr int RL = 16;
   static constexpr int R = 2 * W;
@@ -147,12 +148,11 @@ struct FwdPairCfg {
   static constexpr size_t smem = 2 * raw_bytes + pair_bytes + sizeof(float) * 3 * R * kN;
 };
 
-template <typename Io, int W, int KT, bool kSplit>
+template <typename Io, int W, int KT>
 __global__ void __launch_bounds__(W * 32)
     scan_fwd_pair_kernel(ScanArgs p, typename Io::T* __restrict__ y_out, float* __restrict__ h_last) {
   using T = typename Io::T;
   using Cfg = FwdPairCfg<Io, W, KT>;
-  constexpr int H = KT / 2;
   constexpr int RL = Cfg::RL, R = Cfg::R, NT = Cfg::NT, CH = Cfg::CH;
   extern __shared__ float4 smem4[];
   T* raw0 = reinterpret_cast<T*>(smem4);
@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(W * 32)
     load_raw<Io, KT>(urow, ts + CH, L, valid, ru);  // next chunk
     load_raw<Io, KT>(drow, ts + CH, L, valid, rd);
 
-    float dsum = 0.f, dlo = 0.f;
+    float dsum = 0.f;
 #pragma unroll
     for (int i = 0; i < KT; ++i) {
       const float x = dl[i] + bias;
@@ -223,7 +223,6 @@ __global__ void __launch_bounds__(W * 32)
       y[i] = Dd * du[i];
       du[i] = dt * du[i];
       dsum += dt;
-      if (i == H - 1) dlo = dsum;
     }
 
 #pragma unroll 1
@@ -244,61 +243,24 @@ __global__ void __launch_bounds__(W * 32)
         bb[2 * k] = make_float2(du[2 * k] * v.x, du[2 * k] * v.y);
         bb[2 * k + 1] = make_float2(du[2 * k + 1] * v.z, du[2 * k + 1] * v.w);
       }
-      if constexpr (!kSplit) {
-        float2 S = bb[0];
+      float2 S = bb[0];
 #pragma unroll
-        for (int i = 1; i < KT; ++i) S = fma2(a[i], S, bb[i]);
-        const float2 ps = mul2(make_float2(dsum, dsum), a2);
-        float2 P = make_float2(ex2f(ps.x), ex2f(ps.y));
-        scan_pair_fwd<RL, 2>(P, S, j);
-        hout = fma2(P, hc, S);  // state after this lane's segment
-        float2 h;
-        h.x = __shfl_up_sync(0xffffffffu, hout.x, 2);
-        h.y = __shfl_up_sync(0xffffffffu, hout.y, 2);
-        if (j == 0) h = hc;
+      for (int i = 1; i < KT; ++i) S = fma2(a[i], S, bb[i]);
+      const float2 ps = mul2(make_float2(dsum, dsum), a2);
+      float2 P = make_float2(ex2f(ps.x), ex2f(ps.y));
+      scan_pair_fwd<RL, 2>(P, S, j);
+      hout = fma2(P, hc, S);  // state after this lane's segment
+      float2 h;
+      h.x = __shfl_up_sync(0xffffffffu, hout.x, 2);
+      h.y = __shfl_up_sync(0xffffffffu, hout.y, 2);
+      if (j == 0) h = hc;
 #pragma unroll
-        for (int k = 0; k < KT / 2; ++k) {
-          const float4 c = cq[k * RL];
-          h = fma2(a[2 * k], h, bb[2 * k]);
-          y[2 * k] = fmaf(c.y, h.y, fmaf(c.x, h.x, y[2 * k]));
-          h = fma2(a[2 * k + 1], h, bb[2 * k + 1]);
-          y[2 * k + 1] = fmaf(c.w, h.y, fmaf(c.z, h.x, y[2 * k + 1]));
-        }
-      } else {
-        // two half-segment folds and replays, run side by side
-        float2 Slo = bb[0], Shi = bb[H];
-#pragma unroll
-        for (int i = 1; i < H; ++i) {
-          Slo = fma2(a[i], Slo, bb[i]);
-          Shi = fma2(a[H + i], Shi, bb[H + i]);
-        }
-        const float2 pl = mul2(make_float2(dlo, dlo), a2);
-        const float2 ph = mul2(make_float2(dsum - dlo, dsum - dlo), a2);
-        const float2 ps = mul2(make_float2(dsum, dsum), a2);
-        const float2 Plo = make_float2(ex2f(pl.x), ex2f(pl.y));
-        const float2 Phi = make_float2(ex2f(ph.x), ex2f(ph.y));
-        float2 P = make_float2(ex2f(ps.x), ex2f(ps.y));
-        float2 S = fma2(Phi, Slo, Shi);
-        scan_pair_fwd<RL, 2>(P, S, j);
-        hout = fma2(P, hc, S);
-        float2 h;
-        h.x = __shfl_up_sync(0xffffffffu, hout.x, 2);
-        h.y = __shfl_up_sync(0xffffffffu, hout.y, 2);
-        if (j == 0) h = hc;
-        float2 h2 = fma2(Plo, h, Slo);  // state entering the second half
-#pragma unroll
-        for (int k = 0; k < H / 2; ++k) {
-          const float4 c = cq[k * RL];
-          const float4 c2 = cq[(k + H / 2) * RL];
-          h = fma2(a[2 * k], h, bb[2 * k]);
-          h2 = fma2(a[H + 2 * k], h2, bb[H + 2 * k]);
-          y[2 * k] = fmaf(c.y, h.y, fmaf(c.x, h.x, y[2 * k]));
-          y[H + 2 * k] = fmaf(c2.y, h2.y, fmaf(c2.x, h2.x, y[H + 2 * k]));
-          h = fma2(a[2 * k + 1], h, bb[2 * k + 1]);
-          h2 = fma2(a[H + 2 * k + 1], h2, bb[H + 2 * k + 1]);
-          y[2 * k + 1] = fmaf(c.w, h.y, fmaf(c.z, h.x, y[2 * k + 1]));
-          y[H + 2 * k + 1] = fmaf(c2.w, h2.y, fmaf(c2.z, h2.x, y[H + 2 * k + 1]));
-        }
+      for (int k = 0; k < KT / 2; ++k) {
+        const float4 c = cq[k * RL];
+        h = fma2(a[2 * k], h, bb[2 * k]);
+        y[2 * k] = fmaf(c.y, h.y, fmaf(c.x, h.x, y[2 * k]));
+        h = fma2(a[2 * k + 1], h, bb[2 * k + 1]);
+        y[2 * k + 1] = fmaf(c.w, h.y, fmaf(c.z, h.x, y[2 * k + 1]));
       }
       if (j == RL - 1) *reinterpret_cast<float2*>(carry + ((cur ^ 1) * R + r) * kN + 2 * q) = hout;
     }
@@ -318,10 +280,10 @@ __global__ void __launch_bounds__(W * 32)
   }
 }
 
-template <typename Io, int W, int KT, bool kSplit = false>
+template <typename Io, int W, int KT>
 static cudaError_t launch_fwd_pair(const ScanArgs& a, void* y, float* h_last, cudaStream_t s) {
   using Cfg = FwdPairCfg<Io, W, KT>;
-  auto kern = scan_fwd_pair_kernel<Io, W, KT, kSplit>;
+  auto kern = scan_fwd_pair_kernel<Io, W, KT>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::smem);
   if (e != cudaSuccess) return e;
@@ -342,39 +304,17 @@ static cudaError_t launch_fwd_t(const ScanArgs& a, void* y, float* h_last, cudaS
   return cudaGetLastError();
 }
 
-// Variant selector for experiments (0 = default).
-static int fwd_variant() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = getenv("SELSCAN_FWD_VARIANT");
-    v = e ? atoi(e) : 0;
-  }
-  return v;
-}
-
+// Rows of 16-byte multiples take the paired kernel in the configuration that
+// measured fastest for the I/O type (bf16 8 x 1536 x 2048: 4 warps, 16 steps
+// per lane; fp32 8 x 2048 x 2048: 8 warps, 8 steps per lane); other lengths
+// the element-wise kernel.
 cudaError_t launch_scan_fwd(const ScanArgs& a, void* y, float* h_last, cudaStream_t s) {
-  constexpr int W = 8;
-  const int v = fwd_variant();
   if (a.dt == Dt::BF16) {
-    const bool vec = (a.L % IoBf16::kVec) == 0;
-    if (vec && v == 0) return launch_fwd_pair<IoBf16, 4, 16>(a, y, h_last, s);
-    if (vec && v == 2) return launch_fwd_pair<IoBf16, 4, 8>(a, y, h_last, s);
-    if (vec && v == 3) return launch_fwd_pair<IoBf16, 8, 8>(a, y, h_last, s);
-    if (vec && v == 4) return launch_fwd_pair<IoBf16, 8, 16>(a, y, h_last, s);
-    if (vec && v == 5) return launch_fwd_pair<IoBf16, 4, 16, true>(a, y, h_last, s);
-    if (vec && v == 6) return launch_fwd_pair<IoBf16, 8, 8, true>(a, y, h_last, s);
-    return vec ? launch_fwd_t<IoBf16, W, true>(a, y, h_last, s)
-               : launch_fwd_t<IoBf16, W, false>(a, y, h_last, s);
+    if (a.L % IoBf16::kVec == 0) return launch_fwd_pair<IoBf16, 4, 16>(a, y, h_last, s);
+    return launch_fwd_t<IoBf16, 8, false>(a, y, h_last, s);
   }
-  const bool vec = (a.L % IoF32::kVec) == 0;
-  if (vec && v == 0) return launch_fwd_pair<IoF32, 4, 16>(a, y, h_last, s);
-  if (vec && v == 2) return launch_fwd_pair<IoF32, 4, 8>(a, y, h_last, s);
-  if (vec && v == 3) return launch_fwd_pair<IoF32, 8, 8>(a, y, h_last, s);
-  if (vec && v == 4) return launch_fwd_pair<IoF32, 8, 16>(a, y, h_last, s);
-  if (vec && v == 5) return launch_fwd_pair<IoF32, 4, 16, true>(a, y, h_last, s);
-  if (vec && v == 6) return launch_fwd_pair<IoF32, 8, 8, true>(a, y, h_last, s);
-  return vec ? launch_fwd_t<IoF32, W, true>(a, y, h_last, s)
-             : launch_fwd_t<IoF32, W, false>(a, y, h_last, s);
+  if (a.L % IoF32::kVec == 0) return launch_fwd_pair<IoF32, 8, 8>(a, y, h_last, s);
+  return launch_fwd_t<IoF32, 8, false>(a, y, h_last, s);
 }
 
 }  // namespace selscan

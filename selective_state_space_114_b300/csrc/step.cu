@@ -3,10 +3,10 @@
 // lpnh.cn, section 6.2 on streaming with a carried state):
 //   delta = softplus(delta_t + bias); h <- exp(delta A) h + delta B_t u_t;
 //   y_t = (C_t . h + D u_t) silu(z_t)
-// Bandwidth-bound on the float32 state (128 bytes read and written per row):
-// one thread per (batch, channel) row keeps its 16 states in registers, with
-// four 16-byte loads and stores of h in flight; A, B_t and C_t are small and
-// come from the caches.
+// Bandwidth-bound on the float32 state: four threads per (batch, channel) row,
+// each updating four states with one 16-byte load and store, so a warp moves
+// 512 contiguous bytes of h per access; the C.h sum is finished with two
+// shuffles inside the group of four.
 #include "common.cuh"
 #include "launch.h"
 
@@ -15,67 +15,68 @@ namespace selscan {
 namespace {
 
 template <typename Io>
-__device__ __forceinline__ void load16(const typename Io::T* p, float (&v)[kN]) {
+__device__ __forceinline__ void load4(const typename Io::T* p, float (&v)[4]) {
   if constexpr (Io::kVec == 8) {
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(p), v);
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(p + 8), v + 8);
+    const uint2 w = *reinterpret_cast<const uint2*>(p);
+    v[0] = __uint_as_float(w.x << 16);
+    v[1] = __uint_as_float(w.x & 0xffff0000u);
+    v[2] = __uint_as_float(w.y << 16);
+    v[3] = __uint_as_float(w.y & 0xffff0000u);
   } else {
-#pragma unroll
-    for (int k = 0; k < kN / 4; ++k) {
-      const float4 w = *reinterpret_cast<const float4*>(p + 4 * k);
-      v[4 * k] = w.x;
-      v[4 * k + 1] = w.y;
-      v[4 * k + 2] = w.z;
-      v[4 * k + 3] = w.w;
-    }
+    const float4 w = *reinterpret_cast<const float4*>(p);
+    v[0] = w.x;
+    v[1] = w.y;
+    v[2] = w.z;
+    v[3] = w.w;
   }
 }
 
 template <typename Io>
 __global__ void __launch_bounds__(256) step_kernel(StepArgs p) {
   using T = typename Io::T;
-  const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (row >= p.Bsz * p.Dch) return;
-  const int64_t b = row / p.Dch, d = row % p.Dch;
-  float4* hp = reinterpret_cast<float4*>(p.h + row * kN);
-  float4 h4[kN / 4];
-#pragma unroll
-  for (int k = 0; k < kN / 4; ++k) h4[k] = hp[k];
-  const float uu = Io::to_f(static_cast<const T*>(p.u)[row]);
-  const float x = Io::to_f(static_cast<const T*>(p.delta)[row]) +
-                  (p.delta_bias ? p.delta_bias[d] : 0.f);
-  const float dt = p.softplus ? softplus_fast(x) : x;
-  const float zz = p.z ? Io::to_f(static_cast<const T*>(p.z)[row]) : 0.f;
-  const float Dd = p.D ? p.D[d] : 0.f;
-  float Bv[kN], Cv[kN];
-  load16<Io>(static_cast<const T*>(p.B) + b * kN, Bv);
-  load16<Io>(static_cast<const T*>(p.C) + b * kN, Cv);
-  const float4* Ap = reinterpret_cast<const float4*>(p.A + d * kN);
-  const float dtu = dt * uu;
-  float y = Dd * uu;
-#pragma unroll
-  for (int k = 0; k < kN / 4; ++k) {
-    const float4 a = Ap[k];
-    float4 hv = h4[k];
-    hv.x = fmaf(ex2f(dt * a.x * kLog2e), hv.x, dtu * Bv[4 * k]);
-    hv.y = fmaf(ex2f(dt * a.y * kLog2e), hv.y, dtu * Bv[4 * k + 1]);
-    hv.z = fmaf(ex2f(dt * a.z * kLog2e), hv.z, dtu * Bv[4 * k + 2]);
-    hv.w = fmaf(ex2f(dt * a.w * kLog2e), hv.w, dtu * Bv[4 * k + 3]);
-    hp[k] = hv;
-    y = fmaf(Cv[4 * k], hv.x, y);
-    y = fmaf(Cv[4 * k + 1], hv.y, y);
-    y = fmaf(Cv[4 * k + 2], hv.z, y);
-    y = fmaf(Cv[4 * k + 3], hv.w, y);
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t rows = p.Bsz * p.Dch;
+  const int64_t row = gid >> 2;
+  const int q = threadIdx.x & 3;  // states 4q .. 4q+3
+  const bool valid = row < rows;
+  const int64_t rr = valid ? row : 0;
+  const int64_t b = rr / p.Dch, d = rr % p.Dch;
+
+  float yp = 0.f, uu = 0.f, zz = 0.f;
+  float4 hv = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (valid) {
+    uu = Io::to_f(static_cast<const T*>(p.u)[rr]);
+    const float x = Io::to_f(static_cast<const T*>(p.delta)[rr]) +
+                    (p.delta_bias ? p.delta_bias[d] : 0.f);
+    const float dt = p.softplus ? softplus_fast(x) : x;
+    const float4 Av = *reinterpret_cast<const float4*>(p.A + d * kN + 4 * q);
+    float Bv[4], Cv[4];
+    load4<Io>(static_cast<const T*>(p.B) + b * kN + 4 * q, Bv);
+    load4<Io>(static_cast<const T*>(p.C) + b * kN + 4 * q, Cv);
+    hv = *reinterpret_cast<const float4*>(p.h + rr * kN + 4 * q);
+    const float dtu = dt * uu;
+    hv.x = fmaf(ex2f(dt * Av.x * kLog2e), hv.x, dtu * Bv[0]);
+    hv.y = fmaf(ex2f(dt * Av.y * kLog2e), hv.y, dtu * Bv[1]);
+    hv.z = fmaf(ex2f(dt * Av.z * kLog2e), hv.z, dtu * Bv[2]);
+    hv.w = fmaf(ex2f(dt * Av.w * kLog2e), hv.w, dtu * Bv[3]);
+    *reinterpret_cast<float4*>(p.h + rr * kN + 4 * q) = hv;
+    yp = fmaf(Cv[0], hv.x, fmaf(Cv[1], hv.y, fmaf(Cv[2], hv.z, Cv[3] * hv.w)));
+    if (p.z) zz = Io::to_f(static_cast<const T*>(p.z)[rr]);
   }
-  if (p.z) y *= zz * sigmoid_f(zz);
-  static_cast<T*>(p.y)[row] = Io::from_f(y);
+  yp += __shfl_xor_sync(0xffffffffu, yp, 1);
+  yp += __shfl_xor_sync(0xffffffffu, yp, 2);
+  if (valid && q == 0) {
+    float y = fmaf(p.D ? p.D[d] : 0.f, uu, yp);
+    if (p.z) y *= zz * sigmoid_f(zz);
+    static_cast<T*>(p.y)[rr] = Io::from_f(y);
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_step(const StepArgs& a, cudaStream_t s) {
-  const int64_t rows = a.Bsz * a.Dch;
-  const unsigned blocks = (unsigned)((rows + 255) / 256);
+  const int64_t threads = a.Bsz * a.Dch * 4;
+  const unsigned blocks = (unsigned)((threads + 255) / 256);
   if (a.dt == Dt::BF16)
     step_kernel<IoBf16><<<blocks, 256, 0, s>>>(a);
   else
