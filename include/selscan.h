@@ -29,7 +29,7 @@
  *       A, dA                              : [Dch][N]        float32
  *       D, delta_bias, dD, ddelta_bias     : [Dch]           float32
  *       h, h_last                          : [Bsz][Dch][N]   float32
- *     The I/O dtype (ss_dtype) is float32 or bf16 (uint16 bit patterns);
+ *     The I/O dtype (ss_dtype) is float32, bf16 or fp16 (16-bit patterns);
  *     arithmetic is float32 throughout, the state h is always float32.
  *   - Every pointer must be 16-byte aligned (SS_ERR_ALIGN otherwise).  Any
  *     L >= 0 is accepted; rows whose byte length is a multiple of 16 take the
@@ -57,7 +57,9 @@ extern "C" {
 /* Same type as cudaStream_t. */
 typedef struct CUstream_st* ss_stream_t;
 
-typedef enum { SS_F32 = 0, SS_BF16 = 1 } ss_dtype;
+/* I/O element type.  SS_BF16 and SS_F16 arrays hold the 16-bit patterns
+ * (bfloat16 / IEEE binary16); outputs in them are rounded to nearest even. */
+typedef enum { SS_F32 = 0, SS_BF16 = 1, SS_F16 = 2 } ss_dtype;
 
 typedef enum {
     SS_OK = 0,

@@ -30,7 +30,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libselscan.so")
 
-SS_F32, SS_BF16 = 0, 1
+SS_F32, SS_BF16, SS_F16 = 0, 1, 2
 N_STATE = 16
 
 
@@ -102,7 +102,9 @@ def _dtype_code(t: torch.Tensor) -> int:
         return SS_F32
     if t.dtype == torch.bfloat16:
         return SS_BF16
-    raise TypeError(f"I/O dtype must be float32 or bfloat16, got {t.dtype}")
+    if t.dtype == torch.float16:
+        return SS_F16
+    raise TypeError(f"I/O dtype must be float32, bfloat16 or float16, got {t.dtype}")
 
 
 def _ptr(t):

@@ -25,6 +25,10 @@ bool product_too_big(int64_t a, int64_t b, int64_t c) {
 
 ss_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SS_OK : SS_ERR_CUDA; }
 
+bool known_dtype(ss_dtype d) { return d == SS_F32 || d == SS_BF16 || d == SS_F16; }
+
+Dt to_dt(ss_dtype d) { return d == SS_BF16 ? Dt::BF16 : d == SS_F16 ? Dt::F16 : Dt::F32; }
+
 }  // namespace
 
 extern "C" {
@@ -52,7 +56,7 @@ ss_status ss_scan_fwd(const void* u, const void* delta, const float* A, const vo
                       const void* C, const float* D, const void* z, const float* delta_bias,
                       int softplus, int64_t Bsz, int64_t Dch, int64_t L, int64_t N,
                       ss_dtype dtype, void* y, float* h_last, ss_stream_t stream) {
-  if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_DTYPE;
+  if (!known_dtype(dtype)) return SS_ERR_DTYPE;
   if (bad_size(Bsz) || bad_size(Dch) || bad_size(L) || bad_size(N)) return SS_ERR_SHAPE;
   if (Bsz > 65535 || product_too_big(Bsz, Dch, L)) return SS_ERR_SHAPE;
   if (N != 16) return SS_ERR_N_UNSUPPORTED;
@@ -69,14 +73,14 @@ ss_status ss_scan_fwd(const void* u, const void* delta, const float* A, const vo
     return SS_OK;
   }
   selscan::ScanArgs a{u, delta, A, B, C, D, z, delta_bias, softplus ? 1 : 0,
-                      Bsz, Dch, L, dtype == SS_BF16 ? Dt::BF16 : Dt::F32};
+                      Bsz, Dch, L, to_dt(dtype)};
   return cuda_status(selscan::launch_scan_fwd(a, y, h_last, s));
 }
 
 ss_status ss_scan_bwd_workspace_size(int64_t Bsz, int64_t Dch, int64_t L, int64_t N,
                                      ss_dtype dtype, size_t* bytes) {
   if (!bytes) return SS_ERR_NULL;
-  if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_DTYPE;
+  if (!known_dtype(dtype)) return SS_ERR_DTYPE;
   if (bad_size(Bsz) || bad_size(Dch) || bad_size(L) || bad_size(N)) return SS_ERR_SHAPE;
   if (Bsz > 65535 || product_too_big(Bsz, Dch, L)) return SS_ERR_SHAPE;
   if (N != 16) return SS_ERR_N_UNSUPPORTED;
@@ -95,7 +99,7 @@ ss_status check_bwd(const void* u, const void* delta, const float* A, const void
                     ss_dtype dtype, void* du, void* ddelta, float* dA, float* dB, float* dC,
                     float* dD, void* dz, float* ddelta_bias, void* workspace,
                     size_t workspace_bytes, bool* work) {
-  if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_DTYPE;
+  if (!known_dtype(dtype)) return SS_ERR_DTYPE;
   if (bad_size(Bsz) || bad_size(Dch) || bad_size(L) || bad_size(N)) return SS_ERR_SHAPE;
   if (Bsz > 65535 || product_too_big(Bsz, Dch, L)) return SS_ERR_SHAPE;
   if (N != 16) return SS_ERR_N_UNSUPPORTED;
@@ -152,7 +156,7 @@ ss_status run_bwd(int phase, const void* u, const void* delta, const float* A, c
     return SS_OK;
   }
   selscan::ScanArgs a{u, delta, A, B, C, D, z, delta_bias, softplus ? 1 : 0,
-                      Bsz, Dch, L, dtype == SS_BF16 ? Dt::BF16 : Dt::F32};
+                      Bsz, Dch, L, to_dt(dtype)};
   selscan::BwdOut o{dy, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias};
   for (int ph = 0; ph < 3; ++ph) {
     if (phase >= 0 && ph != phase) continue;
@@ -183,7 +187,7 @@ ss_status ss_step(float* h, const void* u_t, const void* delta_t, const float* A
                   const void* B_t, const void* C_t, const float* D, const void* z_t,
                   const float* delta_bias, int softplus, int64_t Bsz, int64_t Dch, int64_t N,
                   ss_dtype dtype, void* y_t, ss_stream_t stream) {
-  if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_DTYPE;
+  if (!known_dtype(dtype)) return SS_ERR_DTYPE;
   if (bad_size(Bsz) || bad_size(Dch) || bad_size(N)) return SS_ERR_SHAPE;
   if (product_too_big(Bsz, Dch, 4)) return SS_ERR_SHAPE;
   if (N != 16) return SS_ERR_N_UNSUPPORTED;
@@ -194,7 +198,7 @@ ss_status ss_step(float* h, const void* u_t, const void* delta_t, const float* A
       misaligned(delta_bias) || misaligned(y_t))
     return SS_ERR_ALIGN;
   selscan::StepArgs a{h, u_t, delta_t, A, B_t, C_t, D, z_t, delta_bias, softplus ? 1 : 0,
-                      Bsz, Dch, dtype == SS_BF16 ? Dt::BF16 : Dt::F32, y_t};
+                      Bsz, Dch, to_dt(dtype), y_t};
   return cuda_status(selscan::launch_step(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

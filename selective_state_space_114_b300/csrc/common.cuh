@@ -13,6 +13,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -50,25 +51,6 @@ __device__ __forceinline__ float sigmoid_f(float x) {
   return rcpf_approx(1.f + ex2f(-x * kLog2e));
 }
 
-// ---------------------------------------------------------------------------
-// I/O element types.
-// ---------------------------------------------------------------------------
-struct IoF32 {
-  using T = float;
-  static constexpr int kVec = 4;  // elements per 16-byte vector
-  __device__ __forceinline__ static float to_f(T v) { return v; }
-  __device__ __forceinline__ static T from_f(float v) { return v; }
-};
-
-struct IoBf16 {
-  using T = uint16_t;  // bf16 bit pattern
-  static constexpr int kVec = 8;
-  __device__ __forceinline__ static float to_f(T v) { return __uint_as_float((uint32_t)v << 16); }
-  __device__ __forceinline__ static T from_f(float v) {
-    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
-  }
-};
-
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 r;
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -97,6 +79,67 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// ---------------------------------------------------------------------------
+// I/O element types: the element type T, the elements per 16-byte vector
+// kVec, scalar conversions, and the conversion of one 16-byte vector to and
+// from kVec floats (round to nearest even on the way out).
+// ---------------------------------------------------------------------------
+struct IoF32 {
+  using T = float;
+  static constexpr int kVec = 4;
+  __device__ __forceinline__ static float to_f(T v) { return v; }
+  __device__ __forceinline__ static T from_f(float v) { return v; }
+  __device__ __forceinline__ static void unpack(uint4 w, float* f) {
+    f[0] = __uint_as_float(w.x);
+    f[1] = __uint_as_float(w.y);
+    f[2] = __uint_as_float(w.z);
+    f[3] = __uint_as_float(w.w);
+  }
+  __device__ __forceinline__ static uint4 pack(const float* f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+};
+
+struct IoBf16 {
+  using T = uint16_t;  // bf16 bit pattern
+  static constexpr int kVec = 8;
+  __device__ __forceinline__ static float to_f(T v) { return __uint_as_float((uint32_t)v << 16); }
+  __device__ __forceinline__ static T from_f(float v) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  }
+  __device__ __forceinline__ static void unpack(uint4 w, float* f) { unpack_bf16x8(w, f); }
+  __device__ __forceinline__ static uint4 pack(const float* f) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+  }
+};
+
+struct IoF16 {
+  using T = uint16_t;  // IEEE binary16 bit pattern
+  static constexpr int kVec = 8;
+  __device__ __forceinline__ static float to_f(T v) { return __half2float(__ushort_as_half(v)); }
+  __device__ __forceinline__ static T from_f(float v) { return __half_as_ushort(__float2half_rn(v)); }
+  __device__ __forceinline__ static void unpack(uint4 w, float* f) {
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&ws[i]));
+      f[2 * i] = v.x;
+      f[2 * i + 1] = v.y;
+    }
+  }
+  __device__ __forceinline__ static uint4 pack(const float* f) {
+    uint32_t r[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 v = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+      r[i] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+  }
+};
+
 // Load kT consecutive elements row[t], t in [t, t + kT), as float; elements
 // at or past L (or all of them when !valid) read as 0.  kVec: the caller
 // guarantees 16-byte alignment of row + t whenever t + kT <= L.
@@ -109,19 +152,9 @@ __device__ __forceinline__ void load_seg(const typename Io::T* row, int64_t t, i
     return;
   }
   if (kVec && t + kT <= L) {
-    if constexpr (Io::kVec == 8) {
+    constexpr int V = Io::kVec;
 #pragma unroll
-      for (int q = 0; q < kT / 8; ++q) unpack_bf16x8(ldg_nc_v4(row + t + 8 * q), v + 8 * q);
-    } else {
-#pragma unroll
-      for (int q = 0; q < kT / 4; ++q) {
-        uint4 w = ldg_nc_v4(row + t + 4 * q);
-        v[4 * q] = __uint_as_float(w.x);
-        v[4 * q + 1] = __uint_as_float(w.y);
-        v[4 * q + 2] = __uint_as_float(w.z);
-        v[4 * q + 3] = __uint_as_float(w.w);
-      }
-    }
+    for (int q = 0; q < kT / V; ++q) Io::unpack(ldg_nc_v4(row + t + V * q), v + V * q);
   } else {
 #pragma unroll
     for (int i = 0; i < kT; ++i) v[i] = (t + i < L) ? Io::to_f(__ldg(row + t + i)) : 0.f;
@@ -134,24 +167,9 @@ __device__ __forceinline__ void store_seg(typename Io::T* row, int64_t t, int64_
                                           const float (&v)[kT]) {
   if (!valid) return;
   if (kVec && t + kT <= L) {
-    if constexpr (Io::kVec == 8) {
+    constexpr int V = Io::kVec;
 #pragma unroll
-      for (int q = 0; q < kT / 8; ++q) {
-        uint4 w;
-        w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-        w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-        w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-        w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-        stg_v4(row + t + 8 * q, w);
-      }
-    } else {
-#pragma unroll
-      for (int q = 0; q < kT / 4; ++q) {
-        uint4 w = make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
-                             __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3]));
-        stg_v4(row + t + 4 * q, w);
-      }
-    }
+    for (int q = 0; q < kT / V; ++q) stg_v4(row + t + V * q, Io::pack(v + V * q));
   } else {
 #pragma unroll
     for (int i = 0; i < kT; ++i)
@@ -188,15 +206,7 @@ __device__ __forceinline__ void stage_bc(const typename Io::T* __restrict__ Bb,
       float* dst = (which ? Cs : Bs) + n * kChunk;
       float f[V];
       if (t0 + tl + V <= L) {
-        uint4 w = ldg_nc_v4(src);
-        if constexpr (V == 8) {
-          unpack_bf16x8(w, f);
-        } else {
-          f[0] = __uint_as_float(w.x);
-          f[1] = __uint_as_float(w.y);
-          f[2] = __uint_as_float(w.z);
-          f[3] = __uint_as_float(w.w);
-        }
+        Io::unpack(ldg_nc_v4(src), f);
       } else {
 #pragma unroll
         for (int e = 0; e < V; ++e) f[e] = (t0 + tl + e < L) ? Io::to_f(src[e]) : 0.f;
@@ -431,17 +441,10 @@ __device__ __forceinline__ void raw_to_pairs(const typename Io::T* raw, float4* 
     const typename Io::T* r0 = raw + (w * kN + 2 * q) * CH + 8 * o;
     const typename Io::T* r1 = r0 + CH;
     float v0[8], v1[8];
-    if constexpr (Io::kVec == 8) {
-      unpack_bf16x8(*reinterpret_cast<const uint4*>(r0), v0);
-      unpack_bf16x8(*reinterpret_cast<const uint4*>(r1), v1);
-    } else {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float4 a = *reinterpret_cast<const float4*>(r0 + 4 * h);
-        const float4 b = *reinterpret_cast<const float4*>(r1 + 4 * h);
-        v0[4 * h] = a.x; v0[4 * h + 1] = a.y; v0[4 * h + 2] = a.z; v0[4 * h + 3] = a.w;
-        v1[4 * h] = b.x; v1[4 * h + 1] = b.y; v1[4 * h + 2] = b.z; v1[4 * h + 3] = b.w;
-      }
+    for (int h = 0; h < 8 / Io::kVec; ++h) {
+      Io::unpack(*reinterpret_cast<const uint4*>(r0 + Io::kVec * h), v0 + Io::kVec * h);
+      Io::unpack(*reinterpret_cast<const uint4*>(r1 + Io::kVec * h), v1 + Io::kVec * h);
     }
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
@@ -484,15 +487,7 @@ __device__ __forceinline__ void load_kt(const typename Io::T* row, int64_t t, in
 #pragma unroll
     for (int q = 0; q < KT / V; ++q) {
       const bool in = valid && (t + V * q < L);
-      uint4 w = in ? ldg_nc_v4(row + t + V * q) : make_uint4(0, 0, 0, 0);
-      if constexpr (V == 8) {
-        unpack_bf16x8(w, v + 8 * q);
-      } else {
-        v[4 * q] = __uint_as_float(w.x);
-        v[4 * q + 1] = __uint_as_float(w.y);
-        v[4 * q + 2] = __uint_as_float(w.z);
-        v[4 * q + 3] = __uint_as_float(w.w);
-      }
+      Io::unpack(in ? ldg_nc_v4(row + t + V * q) : make_uint4(0, 0, 0, 0), v + V * q);
     }
   } else {
 #pragma unroll
@@ -521,16 +516,7 @@ template <typename Io, int KT>
 __device__ __forceinline__ void decode_raw(const RawSeg<Io, KT>& r, float (&v)[KT]) {
   constexpr int V = Io::kVec;
 #pragma unroll
-  for (int q = 0; q < KT / V; ++q) {
-    if constexpr (V == 8) {
-      unpack_bf16x8(r.w[q], v + 8 * q);
-    } else {
-      v[4 * q] = __uint_as_float(r.w[q].x);
-      v[4 * q + 1] = __uint_as_float(r.w[q].y);
-      v[4 * q + 2] = __uint_as_float(r.w[q].z);
-      v[4 * q + 3] = __uint_as_float(r.w[q].w);
-    }
-  }
+  for (int q = 0; q < KT / V; ++q) Io::unpack(r.w[q], v + V * q);
 }
 
 // Store KT values at row[t ..) (elements below L only).
@@ -543,17 +529,7 @@ __device__ __forceinline__ void store_kt(typename Io::T* row, int64_t t, int64_t
 #pragma unroll
     for (int q = 0; q < KT / V; ++q) {
       if (t + V * q >= L) continue;
-      uint4 w;
-      if constexpr (V == 8) {
-        w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-        w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-        w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-        w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-      } else {
-        w = make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
-                       __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3]));
-      }
-      stg_v4(row + t + V * q, w);
+      stg_v4(row + t + V * q, Io::pack(v + V * q));
     }
   } else {
 #pragma unroll

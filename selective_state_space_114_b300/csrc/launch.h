@@ -7,7 +7,7 @@
 
 namespace selscan {
 
-enum class Dt { F32 = 0, BF16 = 1 };
+enum class Dt { F32 = 0, BF16 = 1, F16 = 2 };
 
 struct ScanArgs {
   const void* u;

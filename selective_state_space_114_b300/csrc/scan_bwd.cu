@@ -822,6 +822,10 @@ cudaError_t launch_scan_bwd(int phase, const ScanArgs& a, const BwdOut& o, void*
     return (a.L % IoBf16::kVec) == 0 ? launch_bwd_t<IoBf16, true>(phase, a, o, ws, s)
                                      : launch_bwd_t<IoBf16, false>(phase, a, o, ws, s);
   }
+  if (a.dt == Dt::F16) {
+    return (a.L % IoF16::kVec) == 0 ? launch_bwd_t<IoF16, true>(phase, a, o, ws, s)
+                                    : launch_bwd_t<IoF16, false>(phase, a, o, ws, s);
+  }
   return (a.L % IoF32::kVec) == 0 ? launch_bwd_t<IoF32, true>(phase, a, o, ws, s)
                                   : launch_bwd_t<IoF32, false>(phase, a, o, ws, s);
 }

@@ -306,12 +306,16 @@ static cudaError_t launch_fwd_t(const ScanArgs& a, void* y, float* h_last, cudaS
 
 // Rows of 16-byte multiples take the paired kernel in the configuration that
 // measured fastest for the I/O type (bf16 8 x 1536 x 2048: 4 warps, 16 steps
-// per lane; fp32 8 x 2048 x 2048: 8 warps, 8 steps per lane); other lengths
-// the element-wise kernel.
+// per lane, also used for fp16; fp32 8 x 2048 x 2048: 8 warps, 8 steps per
+// lane); other lengths the element-wise kernel.
 cudaError_t launch_scan_fwd(const ScanArgs& a, void* y, float* h_last, cudaStream_t s) {
   if (a.dt == Dt::BF16) {
     if (a.L % IoBf16::kVec == 0) return launch_fwd_pair<IoBf16, 4, 16>(a, y, h_last, s);
     return launch_fwd_t<IoBf16, 8, false>(a, y, h_last, s);
+  }
+  if (a.dt == Dt::F16) {
+    if (a.L % IoF16::kVec == 0) return launch_fwd_pair<IoF16, 4, 16>(a, y, h_last, s);
+    return launch_fwd_t<IoF16, 8, false>(a, y, h_last, s);
   }
   if (a.L % IoF32::kVec == 0) return launch_fwd_pair<IoF32, 8, 8>(a, y, h_last, s);
   return launch_fwd_t<IoF32, 8, false>(a, y, h_last, s);

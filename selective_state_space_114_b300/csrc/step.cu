@@ -16,12 +16,12 @@ namespace {
 
 template <typename Io>
 __device__ __forceinline__ void load4(const typename Io::T* p, float (&v)[4]) {
-  if constexpr (Io::kVec == 8) {
-    const uint2 w = *reinterpret_cast<const uint2*>(p);
-    v[0] = __uint_as_float(w.x << 16);
-    v[1] = __uint_as_float(w.x & 0xffff0000u);
-    v[2] = __uint_as_float(w.y << 16);
-    v[3] = __uint_as_float(w.y & 0xffff0000u);
+  using T = typename Io::T;
+  if constexpr (sizeof(T) == 2) {
+    const uint2 w = *reinterpret_cast<const uint2*>(p);  // four 16-bit elements
+    const T* e = reinterpret_cast<const T*>(&w);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = Io::to_f(e[i]);
   } else {
     const float4 w = *reinterpret_cast<const float4*>(p);
     v[0] = w.x;
@@ -79,6 +79,8 @@ cudaError_t launch_step(const StepArgs& a, cudaStream_t s) {
   const unsigned blocks = (unsigned)((threads + 255) / 256);
   if (a.dt == Dt::BF16)
     step_kernel<IoBf16><<<blocks, 256, 0, s>>>(a);
+  else if (a.dt == Dt::F16)
+    step_kernel<IoF16><<<blocks, 256, 0, s>>>(a);
   else
     step_kernel<IoF32><<<blocks, 256, 0, s>>>(a);
   return cudaGetLastError();

@@ -73,9 +73,12 @@ def _ptr(a: np.ndarray) -> int:
 def normal(seed: int, tid: int, count: int, dtype: str = "f32", start: int = 0) -> np.ndarray:
     """N(0,1) samples for element indices start .. start+count-1 of tensor ``tid``.
 
-    dtype "f32" -> float32 array; "bf16" -> uint16 bf16 bit patterns.
+    dtype "f32" -> float32 array; "bf16" -> uint16 bf16 bit patterns;
+    "f16" -> float16 array (the float32 samples rounded to nearest even).
     """
     l = lib()
+    if dtype == "f16":
+        return normal(seed, tid, count, "f32", start).astype(np.float16)
     if dtype == "f32":
         out = np.empty(count, np.float32)
         fn = l.synth_normal_f32
@@ -104,6 +107,8 @@ def normal_at(seed: int, tid: int, idx: np.ndarray, dtype: str = "f32") -> np.nd
     """N(0,1) samples at arbitrary flat element indices ``idx``."""
     l = lib()
     idx = np.ascontiguousarray(idx, dtype=np.int64).ravel()
+    if dtype == "f16":
+        return normal_at(seed, tid, idx, "f32").astype(np.float16)
     if dtype == "f32":
         out = np.empty(idx.size, np.float32)
         l.synth_normal_f32(seed, tid, _ptr(idx), 0, idx.size, _ptr(out))
@@ -130,8 +135,13 @@ def to_bf16(x: np.ndarray) -> np.ndarray:
     return out
 
 
+def to_f16(x: np.ndarray) -> np.ndarray:
+    """Round to IEEE binary16 (nearest even)."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16)
+
+
 def widen(x: np.ndarray) -> np.ndarray:
-    """Exact float64 copy of a float32 array or of bf16 bit patterns (uint16)."""
+    """Exact float64 copy of a float32 or float16 array or of bf16 bit patterns (uint16)."""
     if x.dtype == np.uint16:
         return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     return np.asarray(x, dtype=np.float64)

@@ -12,19 +12,33 @@ import synth
 # Tolerances (the floating-point bars of the parity tests).
 #  float32 I/O:                 |err| <= 1e-4 + 1e-4 |ref|
 #  bf16 I/O, fp32 accumulation: |err| <= 2e-2 (|ref| + 1e-2), oracle on the same bf16 inputs
+#  fp16 I/O, fp32 accumulation: |err| <= 2.5e-3 (|ref| + 1e-2): the bf16 bound scaled by the
+#    ratio of the two formats' unit roundoffs (2^-11 against 2^-8, about 5x the roundoff each)
 #  gradients kept in float32:   |err| <= 1e-3 (|ref| + rms(ref))
 #  gradients stored in bf16 use the bf16 bound (their own rounding is 2^-9 relative).
 F32_ATOL, F32_RTOL = 1e-4, 1e-4
 BF16_REL, BF16_FLOOR = 2e-2, 1e-2
+F16_REL, F16_FLOOR = 2.5e-3, 1e-2
 GRAD_REL = 1e-3
 
 
 def to_dev(a: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
-    """Generator array (float32, or uint16 bf16 bits) -> CUDA tensor of the I/O dtype."""
+    """Generator array (float32, float16, or uint16 bf16 bits) -> CUDA tensor of the I/O dtype."""
     if dtype == "bf16":
         assert a.dtype == np.uint16
         return torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16).to(device)
+    if dtype == "f16":
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float16)).to(device)
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
+
+
+def as_io(a: np.ndarray, dtype: str) -> np.ndarray:
+    """Round float values to the I/O dtype's host representation."""
+    if dtype == "bf16":
+        return synth.to_bf16(np.asarray(a, dtype=np.float32))
+    if dtype == "f16":
+        return synth.to_f16(a)
+    return np.asarray(a, dtype=np.float32)
 
 
 def to_host64(t: torch.Tensor) -> np.ndarray:
@@ -59,6 +73,8 @@ def check(got, ref, kind: str, what: str):
         bound = F32_ATOL + F32_RTOL * np.abs(ref)
     elif kind == "bf16":
         bound = BF16_REL * (np.abs(ref) + BF16_FLOOR)
+    elif kind == "f16":
+        bound = F16_REL * (np.abs(ref) + F16_FLOOR)
     elif kind == "grad":
         rms = np.sqrt(np.mean(ref ** 2)) if ref.size else 0.0
         bound = GRAD_REL * (np.abs(ref) + rms)
@@ -74,11 +90,11 @@ def check(got, ref, kind: str, what: str):
 
 
 def out_kind(dtype: str) -> str:
-    return "bf16" if dtype == "bf16" else "f32"
+    return dtype if dtype in ("bf16", "f16") else "f32"
 
 
 def grad_kind(dtype: str, stored_in_io: bool) -> str:
-    return "bf16" if (dtype == "bf16" and stored_in_io) else "grad"
+    return dtype if (dtype in ("bf16", "f16") and stored_in_io) else "grad"
 
 
 def oracle_fwd(x: dict, softplus=True, h0=None):

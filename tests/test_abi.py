@@ -103,7 +103,7 @@ def bwd(**kw):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(dtype=2), DTYPE),
+    (dict(dtype=5), DTYPE),
     (dict(N=4), NUNS),
     (dict(L=-5), SHAPE),
     (dict(dy=None), NULL),

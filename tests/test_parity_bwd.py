@@ -5,7 +5,7 @@ import torch
 
 import oracle
 import synth
-from parity_util import (check, grad_kind, inputs_to_dev, make_case, oracle_bwd, to_dev,
+from parity_util import (as_io, check, grad_kind, inputs_to_dev, make_case, oracle_bwd, to_dev,
                          to_host64, widen_all)
 
 import selective_state_space_114_b300 as ss
@@ -39,7 +39,7 @@ def test_tiny_config_f32():
     compare(synth.make_inputs(cfg, with_dy=True), "f32", what="tiny")
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("Bsz,Dch,L", [
     (3, 20, 1000),
     (1, 16, 256),
@@ -54,7 +54,7 @@ def test_shapes(dtype, Bsz, Dch, L):
     compare(x, dtype, what=f"{dtype} {Bsz}x{Dch}x{L}")
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("drop", ["D", "z", "delta_bias", "all", "softplus"])
 def test_optional_inputs(dtype, drop):
     x = make_case(dtype, 2, 18, 520, seed=17, with_dy=True)
@@ -64,7 +64,7 @@ def test_optional_inputs(dtype, drop):
     elif drop == "softplus":
         softplus = False
         d = np.abs(synth.widen(x["delta"])) * 0.05
-        x["delta"] = synth.to_bf16(d.astype(np.float32)) if dtype == "bf16" else d.astype(np.float32)
+        x["delta"] = as_io(d, dtype)
         x["delta_bias"] = np.zeros_like(x["delta_bias"])
     else:
         x[drop] = None
@@ -186,9 +186,9 @@ def test_empty_backward_zero_gradients():
     assert torch.all(out["ddelta_bias"] == 0)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_softplus_extremes_backward(dtype):
     x = make_case(dtype, 2, 20, 390, seed=33, with_dy=True)
     d = synth.widen(x["delta"]) * 20.0
-    x["delta"] = synth.to_bf16(d.astype(np.float32)) if dtype == "bf16" else d.astype(np.float32)
+    x["delta"] = as_io(d, dtype)
     compare(x, dtype, what=f"{dtype} softplus extremes")

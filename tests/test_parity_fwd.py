@@ -5,7 +5,7 @@ import torch
 
 import oracle
 import synth
-from parity_util import (check, inputs_to_dev, make_case, oracle_fwd, out_kind, to_host64,
+from parity_util import (as_io, check, inputs_to_dev, make_case, oracle_fwd, out_kind, to_host64,
                          widen_all)
 
 import selective_state_space_114_b300 as ss
@@ -32,7 +32,7 @@ def test_tiny_config_f32():
     compare(synth.make_inputs(cfg), "f32", what="tiny")
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("Bsz,Dch,L", [
     (3, 20, 1000),   # several chunks + ragged tail, channels not a multiple of the CTA
     (1, 16, 256),    # exactly one chunk
@@ -47,7 +47,7 @@ def test_shapes(dtype, Bsz, Dch, L):
     compare(x, dtype, what=f"{dtype} {Bsz}x{Dch}x{L}")
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("drop", ["D", "z", "delta_bias", "all", "softplus"])
 def test_optional_inputs(dtype, drop):
     x = make_case(dtype, 2, 18, 700, seed=7)
@@ -59,7 +59,7 @@ def test_optional_inputs(dtype, drop):
         # raw deltas must be positive-ish for a decaying state: use |delta| * 0.05
         d = synth.widen(x["delta"])
         d = np.abs(d) * 0.05
-        x["delta"] = synth.to_bf16(d.astype(np.float32)) if dtype == "bf16" else d.astype(np.float32)
+        x["delta"] = as_io(d, dtype)
         x["delta_bias"] = np.zeros_like(x["delta_bias"])
     else:
         x[drop] = None
@@ -78,12 +78,12 @@ def test_empty_inputs():
         assert hl.shape == (Bsz, Dch, 16) and torch.all(hl == 0)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_no_writes_outside_outputs(dtype):
     """Guard regions around y and h_last must be untouched (bounds of every store)."""
     x = make_case(dtype, 2, 19, 300, seed=9)
     xd = inputs_to_dev(x, dtype)
-    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16}.get(dtype, torch.float32)
     pad = 64
     n = 2 * 19 * 300
     ybuf = torch.full((n + 2 * pad,), 7.0, device="cuda", dtype=tdt)
@@ -153,11 +153,36 @@ def test_config3_full_size_sampled_rows():
     _full_config_sampled(3, rows)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_softplus_extremes(dtype):
     """delta_raw spread over about +-60: both branches of the GPU's log1p
     (series below e^-|x| = 1/32, log2 above) and the saturated ends."""
     x = make_case(dtype, 2, 24, 520, seed=31)
     d = synth.widen(x["delta"]) * 20.0
-    x["delta"] = synth.to_bf16(d.astype(np.float32)) if dtype == "bf16" else d.astype(np.float32)
+    x["delta"] = as_io(d, dtype)
     compare(x, dtype, what=f"{dtype} softplus extremes")
+
+
+def test_config2_full_size_forward_sampled_rows():
+    """8 x 2048 x 2048 float32 forward (the fp32 kernel configuration) on sampled rows."""
+    rng = np.random.default_rng(2)
+    rows = [(0, 0), (7, 2047), (4, 1024)] + [(int(rng.integers(8)), int(rng.integers(2048)))
+                                            for _ in range(13)]
+    _full_config_sampled(2, rows)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_zero_step_leaves_only_the_gated_skip(dtype):
+    """delta = 0 without softplus: every decay is 1 and every input term 0, so
+    the state stays 0 and y = D u silu(z) (up to the output rounding)."""
+    x = make_case(dtype, 2, 20, 640, seed=35)
+    x["delta"] = np.zeros_like(x["delta"])
+    x["delta_bias"] = np.zeros_like(x["delta_bias"])
+    xd = inputs_to_dev(x, dtype)
+    y, hl = run_fwd(xd, softplus=False)
+    torch.cuda.synchronize()
+    assert torch.all(hl == 0)
+    w = widen_all(x)
+    z = w["z"]
+    want = w["D"][None, :, None] * w["u"] * z / (1.0 + np.exp(-z))
+    check(to_host64(y), want, out_kind(dtype), f"{dtype} zero step")

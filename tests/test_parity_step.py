@@ -18,7 +18,7 @@ def _params(dtype, Bsz, Dch, seed):
         synth.param_delta_bias(seed, Dch, cfg["dt_range"])
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("Bsz,Dch", [(3, 20), (1, 1), (5, 33)])
 def test_single_steps(dtype, Bsz, Dch):
     cfg, A, D, bias = _params(dtype, Bsz, Dch, 300 + Dch)
@@ -39,7 +39,7 @@ def test_single_steps(dtype, Bsz, Dch):
         check(to_host64(h), href, "f32", f"step {k} h")
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_optional_inputs(dtype):
     cfg, A, D, bias = _params(dtype, 2, 24, 5)
     h = torch.zeros((2, 24, 16), device="cuda")
@@ -54,7 +54,7 @@ def test_optional_inputs(dtype):
     check(to_host64(h), href, "f32", "no D/z/bias h")
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_scan_then_step_equals_longer_scan(dtype):
     """ss_scan_fwd over L1 steps, its final state handed to ss_step for k more
     tokens == the oracle's scan over L1 + k steps."""
