@@ -95,6 +95,25 @@ ss_status ss_scan_fwd(const void* u, const void* delta, const float* A, const vo
                       ss_dtype dtype, void* y, float* h_last, ss_stream_t stream);
 
 /*
+ * Forward selective scan continuing from a given state (chunked prefill, or a
+ * sequence resumed after a previous scan or after decode steps): the scan of
+ * ss_scan_fwd with h_{-1} = h0 instead of 0 ("mamba.py" page, step function of
+ * the 2024-01-17 update and "Mamba 7.9.1", section 6.2: the recurrent form
+ * carries the state from one token or segment to the next).
+ *   h0 [Bsz][Dch][N] float32, nullable (NULL = zero state, i.e. ss_scan_fwd).
+ *   h_last may be the same buffer as h0 (in-place update of a carried state);
+ *   no other overlap between inputs and outputs is allowed.
+ *   L == 0: h_last receives h0 (or zeros).
+ * Everything else (arguments, layouts, checks, status) as ss_scan_fwd.
+ * ss_scan_bwd is the backward of ss_scan_fwd, i.e. of a scan from h_{-1} = 0.
+ */
+ss_status ss_scan_fwd_from_state(const void* u, const void* delta, const float* A,
+                                 const void* B, const void* C, const float* D, const void* z,
+                                 const float* delta_bias, int softplus, const float* h0,
+                                 int64_t Bsz, int64_t Dch, int64_t L, int64_t N, ss_dtype dtype,
+                                 void* y, float* h_last, ss_stream_t stream);
+
+/*
  * Bytes of device workspace ss_scan_bwd needs for these sizes (written to
  * *bytes; 0 is possible).  Pure host computation, no CUDA call.
  */

@@ -55,6 +55,8 @@ def _load() -> ctypes.CDLL:
     lib.ss_version.restype = ci
     lib.ss_scan_fwd.argtypes = [p] * 8 + [ci, i64, i64, i64, i64, ci, p, p, p]
     lib.ss_scan_fwd.restype = ci
+    lib.ss_scan_fwd_from_state.argtypes = [p] * 8 + [ci, p, i64, i64, i64, i64, ci, p, p, p]
+    lib.ss_scan_fwd_from_state.restype = ci
     lib.ss_scan_bwd_workspace_size.argtypes = [i64, i64, i64, i64, ci, ctypes.POINTER(sz)]
     lib.ss_scan_bwd_workspace_size.restype = ci
     lib.ss_scan_bwd.argtypes = ([p] * 8 + [ci, p, i64, i64, i64, i64, ci] + [p] * 8 +
@@ -74,7 +76,8 @@ def _load() -> ctypes.CDLL:
 
 
 _lib = _load()
-EXPORTED_SYMBOLS = ("ss_status_str", "ss_version", "ss_scan_fwd", "ss_scan_bwd_workspace_size",
+EXPORTED_SYMBOLS = ("ss_status_str", "ss_version", "ss_scan_fwd", "ss_scan_fwd_from_state",
+                    "ss_scan_bwd_workspace_size",
                     "ss_scan_bwd", "ss_scan_bwd_states", "ss_scan_bwd_reverse",
                     "ss_scan_bwd_reduce", "ss_step", "ss_scan_bwd_noalloc",
                     "ss_scan_bwd_noalloc_max_scratch")
@@ -146,17 +149,26 @@ def _check_scan_inputs(u, delta, A, B, C, D, z, delta_bias):
 
 
 def ss_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
-                return_last_state=False, out=None, h_last=None):
+                return_last_state=False, out=None, h_last=None, h0=None):
     """Forward selective scan on the current CUDA stream; returns y (and the
-    final state when return_last_state)."""
+    final state when return_last_state).  ``h0``: float32 [Bsz][Dch][N]
+    state to start from (ss_scan_fwd_from_state); ``h_last`` may be ``h0``."""
     Bsz, Dch, L, N = _check_scan_inputs(u, delta, A, B, C, D, z, delta_bias)
     y = torch.empty_like(u) if out is None else out
     if return_last_state and h_last is None:
         h_last = torch.empty((Bsz, Dch, N), device=u.device, dtype=torch.float32)
-    st = _lib.ss_scan_fwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
-                          _ptr(delta_bias), int(bool(softplus)), Bsz, Dch, L, N, _dtype_code(u),
-                          _ptr(y), _ptr(h_last), _stream(u.device))
-    _check("ss_scan_fwd", st)
+    if h0 is None:
+        st = _lib.ss_scan_fwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                              _ptr(delta_bias), int(bool(softplus)), Bsz, Dch, L, N,
+                              _dtype_code(u), _ptr(y), _ptr(h_last), _stream(u.device))
+        _check("ss_scan_fwd", st)
+    else:
+        _same(h0, (Bsz, Dch, N), torch.float32, "h0")
+        st = _lib.ss_scan_fwd_from_state(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                         _ptr(z), _ptr(delta_bias), int(bool(softplus)), _ptr(h0),
+                                         Bsz, Dch, L, N, _dtype_code(u), _ptr(y), _ptr(h_last),
+                                         _stream(u.device))
+        _check("ss_scan_fwd_from_state", st)
     return (y, h_last) if return_last_state else y
 
 

@@ -52,10 +52,12 @@ const char* ss_status_str(ss_status s) {
 
 int ss_version(void) { return 10000; }
 
-ss_status ss_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
-                      const void* C, const float* D, const void* z, const float* delta_bias,
-                      int softplus, int64_t Bsz, int64_t Dch, int64_t L, int64_t N,
-                      ss_dtype dtype, void* y, float* h_last, ss_stream_t stream) {
+namespace {
+
+ss_status run_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                  const float* D, const void* z, const float* delta_bias, int softplus,
+                  const float* h0, int64_t Bsz, int64_t Dch, int64_t L, int64_t N, ss_dtype dtype,
+                  void* y, float* h_last, ss_stream_t stream) {
   if (!known_dtype(dtype)) return SS_ERR_DTYPE;
   if (bad_size(Bsz) || bad_size(Dch) || bad_size(L) || bad_size(N)) return SS_ERR_SHAPE;
   if (Bsz > 65535 || product_too_big(Bsz, Dch, L)) return SS_ERR_SHAPE;
@@ -64,17 +66,40 @@ ss_status ss_scan_fwd(const void* u, const void* delta, const float* A, const vo
   if (work && (!u || !delta || !A || !B || !C || !y)) return SS_ERR_NULL;
   if (misaligned(u) || misaligned(delta) || misaligned(A) || misaligned(B) || misaligned(C) ||
       misaligned(D) || misaligned(z) || misaligned(delta_bias) || misaligned(y) ||
-      misaligned(h_last))
+      misaligned(h_last) || misaligned(h0))
     return SS_ERR_ALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (!work) {
-    if (h_last && Bsz > 0 && Dch > 0)
-      return cuda_status(cudaMemsetAsync(h_last, 0, sizeof(float) * (size_t)(Bsz * Dch * N), s));
+    if (h_last && Bsz > 0 && Dch > 0) {
+      const size_t bytes = sizeof(float) * (size_t)(Bsz * Dch * N);
+      if (!h0) return cuda_status(cudaMemsetAsync(h_last, 0, bytes, s));
+      if (h0 != h_last)
+        return cuda_status(cudaMemcpyAsync(h_last, h0, bytes, cudaMemcpyDeviceToDevice, s));
+    }
     return SS_OK;
   }
   selscan::ScanArgs a{u, delta, A, B, C, D, z, delta_bias, softplus ? 1 : 0,
-                      Bsz, Dch, L, to_dt(dtype)};
+                      Bsz, Dch, L, to_dt(dtype), h0};
   return cuda_status(selscan::launch_scan_fwd(a, y, h_last, s));
+}
+
+}  // namespace
+
+ss_status ss_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
+                      const void* C, const float* D, const void* z, const float* delta_bias,
+                      int softplus, int64_t Bsz, int64_t Dch, int64_t L, int64_t N,
+                      ss_dtype dtype, void* y, float* h_last, ss_stream_t stream) {
+  return run_fwd(u, delta, A, B, C, D, z, delta_bias, softplus, nullptr, Bsz, Dch, L, N, dtype,
+                 y, h_last, stream);
+}
+
+ss_status ss_scan_fwd_from_state(const void* u, const void* delta, const float* A,
+                                 const void* B, const void* C, const float* D, const void* z,
+                                 const float* delta_bias, int softplus, const float* h0,
+                                 int64_t Bsz, int64_t Dch, int64_t L, int64_t N, ss_dtype dtype,
+                                 void* y, float* h_last, ss_stream_t stream) {
+  return run_fwd(u, delta, A, B, C, D, z, delta_bias, softplus, h0, Bsz, Dch, L, N, dtype, y,
+                 h_last, stream);
 }
 
 ss_status ss_scan_bwd_workspace_size(int64_t Bsz, int64_t Dch, int64_t L, int64_t N,

@@ -21,6 +21,7 @@ struct ScanArgs {
   int softplus;
   int64_t Bsz, Dch, L;
   Dt dt;
+  const float* h0 = nullptr;  // forward only: state before step 0, [Bsz][Dch][N] (nullable = 0)
 };
 
 struct BwdOut {

@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(W * 32)
 
   for (int i = tid; i < R * kN; i += NT) {
     const int64_t dd = d0 + i / kN;
-    carry[i] = 0.f;
+    carry[i] = (p.h0 && dd < p.Dch) ? p.h0[(b * p.Dch + dd) * kN + i % kN] : 0.f;
     A2s[i] = dd < p.Dch ? p.A[dd * kN + i % kN] * kLog2e : 0.f;
   }
   const float Dd = (valid && p.D) ? p.D[d] : 0.f;
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(W * 32)
 
   for (int i = tid; i < R * kN; i += NT) {
     const int64_t dd = d0 + i / kN;
-    carry[i] = 0.f;
+    carry[i] = (p.h0 && dd < p.Dch) ? p.h0[(b * p.Dch + dd) * kN + i % kN] : 0.f;
     A2s[i] = dd < p.Dch ? p.A[dd * kN + i % kN] * kLog2e : 0.f;
   }
   const float Dd = (valid && p.D) ? p.D[d] : 0.f;

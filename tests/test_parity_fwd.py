@@ -186,3 +186,51 @@ def test_zero_step_leaves_only_the_gated_skip(dtype):
     z = w["z"]
     want = w["D"][None, :, None] * w["u"] * z / (1.0 + np.exp(-z))
     check(to_host64(y), want, out_kind(dtype), f"{dtype} zero step")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("Bsz,Dch,L", [(2, 20, 700), (1, 17, 37), (3, 9, 256)])
+def test_from_state_matches_oracle(dtype, Bsz, Dch, L):
+    """ss_scan_fwd_from_state against the oracle started from the same h0."""
+    x = make_case(dtype, Bsz, Dch, L, seed=50 + L)
+    h0 = np.random.default_rng(L).standard_normal((Bsz, Dch, 16)).astype(np.float32)
+    xd = inputs_to_dev(x, dtype)
+    y, hl = ss.ss_scan_fwd(xd["u"], xd["delta"], xd["A"], xd["B"], xd["C"], xd["D"], xd["z"],
+                           xd["delta_bias"], True, return_last_state=True,
+                           h0=torch.from_numpy(h0).cuda())
+    torch.cuda.synchronize()
+    ref, href = oracle_fwd(x, True, h0=h0.astype(np.float64))
+    check(to_host64(y), ref, out_kind(dtype), f"{dtype} from state y")
+    check(to_host64(hl), href, "f32" if dtype == "f32" else out_kind(dtype), "from state h_last")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_two_chunks_in_place_equal_one_scan(dtype):
+    """Chunked prefill: scan [0, L1), then continue over [L1, L) from the
+    carried state updated in place (h_last = h0) == one scan over [0, L)."""
+    L1, L = 512, 1200
+    x = make_case(dtype, 2, 18, L, seed=61)
+    xd = inputs_to_dev(x, dtype)
+    part = lambda t, a, b: t[..., a:b].contiguous()
+    y1, h = ss.ss_scan_fwd(*(part(xd[k], 0, L1) for k in ("u", "delta")), xd["A"],
+                           part(xd["B"], 0, L1), part(xd["C"], 0, L1), xd["D"],
+                           part(xd["z"], 0, L1), xd["delta_bias"], True, return_last_state=True)
+    y2, h2 = ss.ss_scan_fwd(*(part(xd[k], L1, L) for k in ("u", "delta")), xd["A"],
+                            part(xd["B"], L1, L), part(xd["C"], L1, L), xd["D"],
+                            part(xd["z"], L1, L), xd["delta_bias"], True,
+                            return_last_state=True, h0=h, h_last=h)
+    torch.cuda.synchronize()
+    assert h2.data_ptr() == h.data_ptr()
+    ref, href = oracle_fwd(x, True)
+    check(to_host64(torch.cat([y1, y2], dim=-1)), ref, out_kind(dtype), f"{dtype} chunked y")
+    check(to_host64(h), href, "f32" if dtype == "f32" else "bf16", "chunked final state")
+
+
+def test_from_state_empty_sequence_copies_the_state():
+    h0 = torch.randn(2, 4, 16, device="cuda")
+    A = torch.full((4, 16), -1.0, device="cuda")
+    u = torch.zeros((2, 4, 0), device="cuda")
+    B = torch.zeros((2, 16, 0), device="cuda")
+    _, hl = ss.ss_scan_fwd(u, u, A, B, B, return_last_state=True, h0=h0)
+    torch.cuda.synchronize()
+    assert torch.equal(hl, h0)
