@@ -381,6 +381,56 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # GPU timing
 # ---------------------------------------------------------------------------
+def _flushed_median_ms(fn, steps, dev):
+    """Median time of fn() with L2 flushed before each call (a 256 MiB read).
+    The GPU first spins for ~25 ms so that the host enqueues every timed call
+    ahead of it: the events then bracket GPU work only, not launch latency."""
+    import torch
+    flush = torch.ones(64 * 2 ** 20, device=dev, dtype=torch.float32)
+    sink = torch.empty((), device=dev, dtype=torch.float32)
+    for _ in range(3):
+        fn()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(50_000_000)
+    for e0, e1 in evs:
+        torch.sum(flush, dim=0, out=sink)
+        e0.record()
+        fn()
+        e1.record()
+    torch.cuda.synchronize()
+    return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+
+
+def conv_measure(ss, dev, seed, steps=16):
+    """The causal depthwise conv1d + silu (width 4) that produces u, forward
+    and backward, on the bench layer's shape (8 x 1536 x 2048, bf16); L2 is
+    flushed before each call.  Returns times and HBM rooflines."""
+    import torch
+    cfg = synth.config(CFG_INDEX)
+    Bsz, Dch, L, K = cfg["Bsz"], cfg["Dch"], cfg["L"], 4
+    E = Bsz * Dch * L
+    bf = torch.bfloat16
+    x = torch.from_numpy(synth.normal(seed, 20, E, "bf16").reshape(Bsz, Dch, L)).view(bf).to(dev)
+    g = torch.from_numpy(synth.normal(seed, 23, E, "bf16").reshape(Bsz, Dch, L)).view(bf).to(dev)
+    w = torch.from_numpy(synth.normal(seed, 21, Dch * K, "f32").reshape(Dch, K) / 2.0).to(dev)
+    b = torch.from_numpy(synth.normal(seed, 22, Dch, "f32")).to(dev)
+    u = torch.empty_like(x)
+    grads = {"dx": torch.empty_like(x), "dw": torch.empty((Dch, K), device=dev),
+             "dbias": torch.empty((Dch,), device=dev)}
+    ms_f = _flushed_median_ms(lambda: ss.ss_conv1d_silu(x, w, b, True, out=u), steps, dev)
+    ms_b = _flushed_median_ms(lambda: ss.ss_conv1d_silu_bwd(x, w, b, True, g, out=grads), steps,
+                              dev)
+    hbm, _ = load_peaks()
+    res = {"workload": f"conv1d (width {K}) + silu, Bsz={Bsz} Dch={Dch} L={L}, bf16, "
+                       f"L2 flushed before each call"}
+    for name, ms, nbytes in (("fwd", ms_f, 2 * 2 * E), ("bwd", ms_b, 3 * 2 * E)):
+        ach = nbytes / (ms * 1e-3) / 1e9
+        res[name] = {"ms": round(ms, 4), "gelem_s": round(E / (ms * 1e-3) / 1e9, 2), "bound": "hbm",
+                     "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(ach / hbm, 4), "algorithmic_bytes": nbytes}
+    return res
 def decode_step_measure(ss, dev, seed, steps=16):
     """The one-token step on the decode workload (Bsz=256, Dch=5120, N=16,
     bf16 tokens, float32 state): its state (84 MB) fits in L2, so L2 is
@@ -403,19 +453,8 @@ def decode_step_measure(ss, dev, seed, steps=16):
     bias = torch.from_numpy(np.ascontiguousarray(x["delta_bias"], dtype=np.float32)).to(dev)
     h = torch.zeros((Bsz, Dch, N), device=dev, dtype=torch.float32)
     y = torch.empty((Bsz, Dch), device=dev, dtype=bf)
-    flush = torch.ones(64 * 2 ** 20, device=dev, dtype=torch.float32)  # 256 MiB
-    sink = torch.empty((), device=dev, dtype=torch.float32)
-    for _ in range(3):
-        ss.ss_step(h, u, dl, A, B, C, D, z, bias, True, out=y)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
-    for e0, e1 in evs:
-        torch.sum(flush, dim=0, out=sink)
-        e0.record()
-        ss.ss_step(h, u, dl, A, B, C, D, z, bias, True, out=y)
-        e1.record()
-    torch.cuda.synchronize()
-    ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+    ms = _flushed_median_ms(lambda: ss.ss_step(h, u, dl, A, B, C, D, z, bias, True, out=y), steps,
+                            dev)
     rows = Bsz * Dch
     nbytes = rows * (2 * N * 4 + 4 * 2) + 2 * Bsz * N * 2  # h in/out, u/delta/z/y, B/C
     hbm, _ = load_peaks()
@@ -424,6 +463,8 @@ def decode_step_measure(ss, dev, seed, steps=16):
                         f"L2 flushed before each step", "ms": round(ms, 4),
             "bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
             "frac": round(ach / hbm, 4), "algorithmic_bytes": nbytes}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -518,6 +559,7 @@ def run_ours(args):
     fwd_gelem = E / (per_kernel["fwd"] * 1e-3) / 1e9
 
     decode = decode_step_measure(ss, dev, seed) if rank == 0 else None
+    conv = conv_measure(ss, dev, seed) if rank == 0 else None
 
     # end to end through the public API with host buffers
     Ke = max(3, min(K, 10))
@@ -563,6 +605,7 @@ def run_ours(args):
                             if nm in roofs else {})} for nm in names},
         "gpu_launches": K * LAUNCHES_PER_STEP,
         "decode_step": decode,
+        "conv1d_silu": conv,
         "e2e": {"value": round(world * E / (e2e_ms * 1e-3) / 1e9, 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 3)},

@@ -192,6 +192,37 @@ ss_status ss_step(float* h, const void* u_t, const void* delta_t, const float* A
                   ss_dtype dtype, void* y_t, ss_stream_t stream);
 
 /*
+ * Causal depthwise conv1d + silu, the step of the Mamba block that produces
+ * the scan input u from the in-projection output x ("Mamba 7.9.1", section
+ * 4.1: d_conv = 4; "mamba.py" page, resources: a plain Conv1d in the minimal
+ * implementation):
+ *   c_t = bias_d + sum_{k<K} w[d][k] x_{t-(K-1)+k}   (x_s = 0 for s < 0)
+ *   u_t = c_t * sigmoid(c_t)                          (c_t when silu == 0)
+ *   in : x [Bsz][Dch][L] (I/O dtype); w [Dch][K] float32; bias [Dch] float32
+ *        (nullable = 0); K = kernel width, 1 .. 4 (SS_ERR_SHAPE otherwise).
+ *   out: u [Bsz][Dch][L] (I/O dtype); must not overlap x.
+ * Conventions as for the scan (device pointers, 16-byte alignment, async on
+ * stream, checks before launch).
+ */
+ss_status ss_conv1d_silu_fwd(const void* x, const float* w, const float* bias, int silu,
+                             int64_t Bsz, int64_t Dch, int64_t L, int64_t K, ss_dtype dtype,
+                             void* u, ss_stream_t stream);
+
+/*
+ * Backward of ss_conv1d_silu_fwd for the upstream gradient du:
+ *   gc_t = du_t silu'(c_t) (du_t when silu == 0);
+ *   dx_s = sum_k w[d][k] gc_{s+(K-1)-k};  dw[d][k] = sum_{b,t} gc_t x_{t-(K-1)+k};
+ *   dbias_d = sum_{b,t} gc_t.
+ *   out: dx [Bsz][Dch][L] (I/O dtype); dw [Dch][K], dbias [Dch] float32 (dbias
+ *        non-NULL iff bias non-NULL).  Sums over (b, t) in a fixed order:
+ *        reruns are bitwise equal.  Empty Bsz or L: dw, dbias set to 0.
+ */
+ss_status ss_conv1d_silu_bwd(const void* x, const float* w, const float* bias, int silu,
+                             const void* du, int64_t Bsz, int64_t Dch, int64_t L, int64_t K,
+                             ss_dtype dtype, void* dx, float* dw, float* dbias,
+                             ss_stream_t stream);
+
+/*
  * Backward scan for callers that cannot allocate device memory.
  *
  * The pages describe no counterpart of this entry point; it exists for

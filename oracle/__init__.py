@@ -75,6 +75,8 @@ class Oracle:
         l.oracle_scan_fwd_blelloch.argtypes = l.oracle_scan_fwd.argtypes
         l.oracle_scan_bwd.argtypes = [p] * 8 + [ci, i64, i64, i64, i64] + [p] * 9 + [ci]
         l.oracle_step.argtypes = [p] * 9 + [ci, i64, i64, i64, p, ci]
+        l.oracle_conv1d_silu.argtypes = [p] * 3 + [ci, i64, i64, i64, i64, p, ci]
+        l.oracle_conv1d_silu_bwd.argtypes = [p] * 3 + [ci, p, i64, i64, i64, i64, p, p, p, ci]
         for f in (l.oracle_scan_fwd, l.oracle_scan_fwd_blelloch, l.oracle_scan_bwd, l.oracle_step):
             f.restype = ci
         self._l = l
@@ -147,6 +149,40 @@ class Oracle:
         return y, h
 
 
+    def conv1d_silu(self, x, w, bias=None, silu=True, nthreads=None):
+        """Causal depthwise conv1d (width K) + silu.  x [Bsz][Dch][L], w [Dch][K],
+        bias [Dch] or None.  Returns u [Bsz][Dch][L]."""
+        x = _f64(x)
+        Bsz, Dch, L = x.shape
+        w = _f64(w)
+        K = w.shape[1]
+        bias = _f64(bias, (Dch,))
+        u = np.empty_like(x)
+        rc = self._l.oracle_conv1d_silu(_p(x), _p(w), _p(bias), int(bool(silu)), Bsz, Dch, L, K,
+                                        _p(u), nthreads or default_threads())
+        if rc:
+            raise RuntimeError(f"oracle conv1d_silu failed ({rc})")
+        return u
+
+    def conv1d_silu_bwd(self, x, w, bias, silu, g, nthreads=None):
+        """Backward of conv1d_silu for upstream gradient g.  Returns dict dx, dw, dbias
+        (dbias None when bias is None)."""
+        x = _f64(x)
+        Bsz, Dch, L = x.shape
+        w = _f64(w)
+        K = w.shape[1]
+        bias = _f64(bias, (Dch,))
+        g = _f64(g, (Bsz, Dch, L))
+        out = {"dx": np.empty_like(x), "dw": np.empty((Dch, K)),
+               "dbias": np.empty(Dch) if bias is not None else None}
+        rc = self._l.oracle_conv1d_silu_bwd(_p(x), _p(w), _p(bias), int(bool(silu)), _p(g), Bsz,
+                                            Dch, L, K, _p(out["dx"]), _p(out["dw"]),
+                                            _p(out["dbias"]), nthreads or default_threads())
+        if rc:
+            raise RuntimeError(f"oracle conv1d_silu_bwd failed ({rc})")
+        return out
+
+
 def default() -> Oracle:
     global _default
     with _lock:
@@ -165,3 +201,11 @@ def scan_bwd(*a, **k):
 
 def step(*a, **k):
     return default().step(*a, **k)
+
+
+def conv1d_silu(*a, **k):
+    return default().conv1d_silu(*a, **k)
+
+
+def conv1d_silu_bwd(*a, **k):
+    return default().conv1d_silu_bwd(*a, **k)

@@ -440,3 +440,96 @@ int oracle_step(double* h, const double* u, const double* delta, const double* A
     run_rows(step_row, &c, Bsz * Dch, nthreads);
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* causal depthwise conv1d + silu (the step that produces u)           */
+/* ------------------------------------------------------------------ */
+/*
+ * The block that feeds the scan: a depthwise causal convolution of width K
+ * (d_conv = 4 in the "Mamba 7.9.1" article, section 4.1; mamba-minimal uses
+ * a torch.nn.Conv1d there, "mamba.py" page, resources section), then silu:
+ *
+ *   c_t = bias_d + sum_{k=0..K-1} w[d][k] x_{t-(K-1)+k}    (x_s = 0 for s < 0)
+ *   u_t = c_t sigmoid(c_t)                                 (c_t when silu == 0)
+ *
+ * Backward, with g = dL/du:  gc_t = g_t silu'(c_t) (or g_t);
+ *   dx_s = sum_k w[d][k] gc_{s+(K-1)-k};  dw[d][k] = sum_{b,t} gc_t x_{t-(K-1)+k};
+ *   dbias_d = sum_{b,t} gc_t.
+ * Layouts: x, u, g, dx [Bsz][Dch][L]; w, dw [Dch][K]; bias, dbias [Dch].
+ */
+typedef struct {
+    const double *x, *w, *bias, *g;
+    int silu;
+    i64 Bsz, Dch, L, K;
+    double *u, *dx, *dw, *dbias;
+} conv_ctx;
+
+static double conv_pre(const conv_ctx* c, const double* xr, i64 d, i64 t) {
+    double s = c->bias ? c->bias[d] : 0.0;
+    for (i64 k = 0; k < c->K; ++k) {
+        const i64 src = t - (c->K - 1) + k;
+        if (src >= 0) s += c->w[d * c->K + k] * xr[src];
+    }
+    return s;
+}
+
+static void conv_fwd_row(void* p, i64 row, int tid) {
+    (void)tid;
+    conv_ctx* c = (conv_ctx*)p;
+    const i64 d = row % c->Dch, L = c->L;
+    const double* xr = c->x + row * L;
+    for (i64 t = 0; t < L; ++t) {
+        const double v = conv_pre(c, xr, d, t);
+        c->u[row * L + t] = c->silu ? v * sigmoid(v) : v;
+    }
+}
+
+int oracle_conv1d_silu(const double* x, const double* w, const double* bias, int silu, i64 Bsz,
+                       i64 Dch, i64 L, i64 K, double* u, int nthreads) {
+    if (K < 1 || Bsz < 0 || Dch < 0 || L < 0) return 1;
+    conv_ctx c = {x, w, bias, NULL, silu, Bsz, Dch, L, K, u, NULL, NULL, NULL};
+    run_rows(conv_fwd_row, &c, Bsz * Dch, nthreads);
+    return 0;
+}
+
+static void conv_bwd_channel(void* p, i64 d, int tid) {
+    (void)tid;
+    conv_ctx* c = (conv_ctx*)p;
+    const i64 L = c->L, K = c->K;
+    double* gc = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+    double db = 0.0;
+    for (i64 k = 0; k < K; ++k) c->dw[d * K + k] = 0.0;
+    for (i64 b = 0; b < c->Bsz; ++b) {
+        const i64 row = b * c->Dch + d;
+        const double* xr = c->x + row * L;
+        for (i64 t = 0; t < L; ++t) {
+            const double v = conv_pre(c, xr, d, t);
+            const double s = sigmoid(v);
+            gc[t] = c->silu ? c->g[row * L + t] * s * (1.0 + v * (1.0 - s)) : c->g[row * L + t];
+            db += gc[t];
+            for (i64 k = 0; k < K; ++k) {
+                const i64 src = t - (K - 1) + k;
+                if (src >= 0) c->dw[d * K + k] += gc[t] * xr[src];
+            }
+        }
+        for (i64 s = 0; s < L; ++s) {
+            double acc = 0.0;
+            for (i64 k = 0; k < K; ++k) {
+                const i64 t = s + (K - 1) - k;
+                if (t < L) acc += c->w[d * K + k] * gc[t];
+            }
+            c->dx[row * L + s] = acc;
+        }
+    }
+    if (c->dbias) c->dbias[d] = db;
+    free(gc);
+}
+
+int oracle_conv1d_silu_bwd(const double* x, const double* w, const double* bias, int silu,
+                           const double* g, i64 Bsz, i64 Dch, i64 L, i64 K, double* dx,
+                           double* dw, double* dbias, int nthreads) {
+    if (K < 1 || Bsz < 0 || Dch < 0 || L < 0) return 1;
+    conv_ctx c = {x, w, bias, g, silu, Bsz, Dch, L, K, NULL, dx, dw, dbias};
+    run_rows(conv_bwd_channel, &c, Dch, nthreads);
+    return 0;
+}

@@ -68,6 +68,10 @@ def _load() -> ctypes.CDLL:
         f.restype = ci
     lib.ss_step.argtypes = [p] * 9 + [ci, i64, i64, i64, ci, p, p]
     lib.ss_step.restype = ci
+    lib.ss_conv1d_silu_fwd.argtypes = [p, p, p, ci, i64, i64, i64, i64, ci, p, p]
+    lib.ss_conv1d_silu_fwd.restype = ci
+    lib.ss_conv1d_silu_bwd.argtypes = [p, p, p, ci, p, i64, i64, i64, i64, ci, p, p, p, p]
+    lib.ss_conv1d_silu_bwd.restype = ci
     lib.ss_scan_bwd_noalloc.argtypes = [p] * 8 + [ci, p, i64, i64, i64, i64, ci] + [p] * 9
     lib.ss_scan_bwd_noalloc.restype = ci
     lib.ss_scan_bwd_noalloc_max_scratch.argtypes = []
@@ -79,7 +83,8 @@ _lib = _load()
 EXPORTED_SYMBOLS = ("ss_status_str", "ss_version", "ss_scan_fwd", "ss_scan_fwd_from_state",
                     "ss_scan_bwd_workspace_size",
                     "ss_scan_bwd", "ss_scan_bwd_states", "ss_scan_bwd_reverse",
-                    "ss_scan_bwd_reduce", "ss_step", "ss_scan_bwd_noalloc",
+                    "ss_scan_bwd_reduce", "ss_step", "ss_conv1d_silu_fwd",
+                    "ss_conv1d_silu_bwd", "ss_scan_bwd_noalloc",
                     "ss_scan_bwd_noalloc_max_scratch")
 
 
@@ -258,3 +263,42 @@ class SelectiveScanFn(torch.autograd.Function):
 def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True):
     """Differentiable selective scan (see SelectiveScanFn)."""
     return SelectiveScanFn.apply(u, delta, A, B, C, D, z, delta_bias, softplus)
+
+
+def ss_conv1d_silu(x, w, bias=None, silu=True, out=None):
+    """Causal depthwise conv1d (width w.shape[1], 1..4) + silu on the current
+    CUDA stream: x [Bsz][Dch][L] (I/O dtype), w [Dch][K] and bias [Dch] float32.
+    Returns u [Bsz][Dch][L]."""
+    if x.dim() != 3 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous [Bsz][Dch][L] tensor")
+    Bsz, Dch, L = x.shape
+    if w.dim() != 2 or w.shape[0] != Dch:
+        raise ValueError("w must be [Dch][K]")
+    K = w.shape[1]
+    _same(w, (Dch, K), torch.float32, "w")
+    if bias is not None:
+        _same(bias, (Dch,), torch.float32, "bias")
+    u = torch.empty_like(x) if out is None else out
+    _check("ss_conv1d_silu_fwd",
+           _lib.ss_conv1d_silu_fwd(_ptr(x), _ptr(w), _ptr(bias), int(bool(silu)), Bsz, Dch, L, K,
+                                   _dtype_code(x), _ptr(u), _stream(x.device)))
+    return u
+
+
+def ss_conv1d_silu_bwd(x, w, bias, silu, du, out=None):
+    """Backward of ss_conv1d_silu for the upstream gradient du.  Returns dict
+    dx, dw, dbias (dbias None when bias is None)."""
+    Bsz, Dch, L = x.shape
+    K = w.shape[1]
+    _same(du, (Bsz, Dch, L), x.dtype, "du")
+    g = out if out is not None else {
+        "dx": torch.empty_like(x),
+        "dw": torch.empty((Dch, K), device=x.device, dtype=torch.float32),
+        "dbias": torch.empty((Dch,), device=x.device, dtype=torch.float32)
+        if bias is not None else None,
+    }
+    _check("ss_conv1d_silu_bwd",
+           _lib.ss_conv1d_silu_bwd(_ptr(x), _ptr(w), _ptr(bias), int(bool(silu)), _ptr(du), Bsz,
+                                   Dch, L, K, _dtype_code(x), _ptr(g["dx"]), _ptr(g["dw"]),
+                                   _ptr(g["dbias"]), _stream(x.device)))
+    return g

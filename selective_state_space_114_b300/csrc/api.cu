@@ -227,4 +227,45 @@ ss_status ss_step(float* h, const void* u_t, const void* delta_t, const float* A
   return cuda_status(selscan::launch_step(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+ss_status ss_conv1d_silu_fwd(const void* x, const float* w, const float* bias, int silu,
+                             int64_t Bsz, int64_t Dch, int64_t L, int64_t K, ss_dtype dtype,
+                             void* u, ss_stream_t stream) {
+  if (!known_dtype(dtype)) return SS_ERR_DTYPE;
+  if (bad_size(Bsz) || bad_size(Dch) || bad_size(L) || K < 1 || K > 4) return SS_ERR_SHAPE;
+  if (product_too_big(Bsz, Dch, L)) return SS_ERR_SHAPE;
+  const bool work = Bsz > 0 && Dch > 0 && L > 0;
+  if (work && (!x || !w || !u)) return SS_ERR_NULL;
+  if (misaligned(x) || misaligned(w) || misaligned(bias) || misaligned(u)) return SS_ERR_ALIGN;
+  if (!work) return SS_OK;
+  selscan::ConvArgs a{x, w, bias, silu ? 1 : 0, Bsz, Dch, L, (int)K, to_dt(dtype), u};
+  selscan::ConvGrads o{nullptr, nullptr, nullptr, nullptr};
+  return cuda_status(selscan::launch_conv(0, a, o, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ss_status ss_conv1d_silu_bwd(const void* x, const float* w, const float* bias, int silu,
+                             const void* du, int64_t Bsz, int64_t Dch, int64_t L, int64_t K,
+                             ss_dtype dtype, void* dx, float* dw, float* dbias,
+                             ss_stream_t stream) {
+  if (!known_dtype(dtype)) return SS_ERR_DTYPE;
+  if (bad_size(Bsz) || bad_size(Dch) || bad_size(L) || K < 1 || K > 4) return SS_ERR_SHAPE;
+  if (product_too_big(Bsz, Dch, L) || Dch > 0x7fffffff) return SS_ERR_SHAPE;
+  const bool work = Bsz > 0 && Dch > 0 && L > 0;
+  if (Dch > 0 && !dw) return SS_ERR_NULL;
+  if (Dch > 0 && (bias != nullptr) != (dbias != nullptr)) return SS_ERR_NULL;
+  if (work && (!x || !w || !du || !dx)) return SS_ERR_NULL;
+  if (misaligned(x) || misaligned(w) || misaligned(bias) || misaligned(du) || misaligned(dx) ||
+      misaligned(dw) || misaligned(dbias))
+    return SS_ERR_ALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!work) {
+    if (Dch == 0) return SS_OK;
+    cudaError_t e = cudaMemsetAsync(dw, 0, sizeof(float) * (size_t)(Dch * K), s);
+    if (e == cudaSuccess && dbias) e = cudaMemsetAsync(dbias, 0, sizeof(float) * (size_t)Dch, s);
+    return cuda_status(e);
+  }
+  selscan::ConvArgs a{x, w, bias, silu ? 1 : 0, Bsz, Dch, L, (int)K, to_dt(dtype), nullptr};
+  selscan::ConvGrads o{du, dx, dw, dbias};
+  return cuda_status(selscan::launch_conv(1, a, o, s));
+}
+
 }  // extern "C"

@@ -65,4 +65,26 @@ cudaError_t launch_scan_bwd(int phase, const ScanArgs& a, const BwdOut& o, void*
 // One decode step.  Requires Bsz*Dch > 0.
 cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
 
+struct ConvArgs {
+  const void* x;
+  const float* w;     // [Dch][K]
+  const float* bias;  // nullable
+  int silu;
+  int64_t Bsz, Dch, L;
+  int K;              // 1 .. 4
+  Dt dt;
+  void* u;            // forward output
+};
+
+struct ConvGrads {
+  const void* g;  // dL/du
+  void* dx;
+  float* dw;
+  float* dbias;   // nullable iff bias null
+};
+
+// Causal depthwise conv1d + silu: phase 0 forward (writes a.u), phase 1
+// backward (writes o.dx, o.dw, o.dbias).  Requires Bsz*Dch*L > 0.
+cudaError_t launch_conv(int phase, const ConvArgs& a, const ConvGrads& o, cudaStream_t s);
+
 }  // namespace selscan

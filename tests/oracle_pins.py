@@ -258,6 +258,74 @@ def pin_bwd_fd_plain(orc, seed=11):
     _fd_check(orc, x, False, dy, "bwd plain")
 
 
+# ---------------------------------------------------------------------------
+# causal depthwise conv1d + silu
+# ---------------------------------------------------------------------------
+def _conv_case(rng, Bsz=2, Dch=3, L=19, K=4):
+    return (rng.standard_normal((Bsz, Dch, L)), rng.standard_normal((Dch, K)),
+            rng.standard_normal(Dch))
+
+
+def pin_conv_convolve(orc, seed=12):
+    """Each row is numpy's full convolution with the flipped taps, first L
+    outputs (left zero padding), plus bias, then x sigmoid(x) (scipy expit)."""
+    rng = np.random.default_rng(seed)
+    for K in (1, 2, 4):
+        x, w, bias = _conv_case(rng, K=K)
+        Bsz, Dch, L = x.shape
+        want = np.empty_like(x)
+        for b in range(Bsz):
+            for d in range(Dch):
+                want[b, d] = np.convolve(x[b, d], w[d][::-1])[:L] + bias[d]
+        _close(orc.conv1d_silu(x, w, bias, silu=False, nthreads=2), want, 1e-13, 1e-14,
+               f"conv K={K}")
+        _close(orc.conv1d_silu(x, w, bias, silu=True, nthreads=2), want * expit(want), 1e-13,
+               1e-14, f"conv+silu K={K}")
+
+
+def pin_conv_lfilter(orc, seed=13):
+    """The causal convolution is the FIR filter lfilter(w reversed, [1], x)."""
+    rng = np.random.default_rng(seed)
+    x, w, _ = _conv_case(rng, Bsz=1, Dch=4, L=33, K=4)
+    got = orc.conv1d_silu(x, w, None, silu=False, nthreads=1)
+    for d in range(4):
+        _close(got[0, d], lfilter(w[d][::-1], [1.0], x[0, d]), 1e-13, 1e-14, "conv lfilter")
+
+
+def pin_conv_impulse(orc, seed=14):
+    """A unit impulse at t0 returns the taps w[K-1], w[K-2], ..., w[0] at t0 .. t0+K-1."""
+    rng = np.random.default_rng(seed)
+    K, L, t0 = 4, 12, 3
+    w = rng.standard_normal((1, K))
+    x = np.zeros((1, 1, L))
+    x[0, 0, t0] = 1.0
+    got = orc.conv1d_silu(x, w, None, silu=False, nthreads=1)[0, 0]
+    want = np.zeros(L)
+    want[t0:t0 + K] = w[0][::-1]
+    _close(got, want, 0, 1e-15, "conv impulse")
+
+
+def pin_conv_bwd_fd(orc, seed=15):
+    """Central differences of sum(g * u) for x, w and bias."""
+    rng = np.random.default_rng(seed)
+    x, w, bias = _conv_case(rng, Bsz=2, Dch=2, L=9, K=4)
+    g = rng.standard_normal(x.shape)
+    got = orc.conv1d_silu_bwd(x, w, bias, True, g, nthreads=1)
+    loss = lambda xx, ww, bb: float(np.sum(g * orc.conv1d_silu(xx, ww, bb, True, nthreads=1)))
+    eps = 1e-6
+    for name, arr in (("dx", x), ("dw", w), ("dbias", bias)):
+        num = np.zeros_like(arr)
+        for i in np.ndindex(arr.shape):
+            hi, lo = arr.copy(), arr.copy()
+            hi[i] += eps
+            lo[i] -= eps
+            args_hi = {"dx": (hi, w, bias), "dw": (x, hi, bias), "dbias": (x, w, hi)}[name]
+            args_lo = {"dx": (lo, w, bias), "dw": (x, lo, bias), "dbias": (x, w, lo)}[name]
+            num[i] = (loss(*args_hi) - loss(*args_lo)) / (2 * eps)
+        _close(got[name], num, 1e-6, 1e-7, f"conv finite differences {name}")
+
+
 ALL_PINS = [pin_closed_form, pin_delta_zero, pin_geometric, pin_lfilter, pin_softplus_cumsum,
             pin_gate_order, pin_blelloch, pin_resume, pin_scan_then_step, pin_bwd_fd,
-            pin_bwd_fd_plain]
+            pin_bwd_fd_plain, pin_conv_convolve, pin_conv_lfilter, pin_conv_impulse,
+            pin_conv_bwd_fd]

@@ -144,3 +144,58 @@ def test_step_rejects(kw, code):
 
 def test_step_empty_is_ok():
     assert step(h=None, u=None, delta=None, A=None, B=None, C=None, y=None, Bsz=0) == OK
+
+
+def fwd_from_state(**kw):
+    a = dict(u=P, delta=P, A=P, B=P, C=P, D=None, z=None, bias=None, softplus=1, h0=P, Bsz=2,
+             Dch=16, L=64, N=16, dtype=0, y=P, h_last=None)
+    a.update(kw)
+    return ss.lib().ss_scan_fwd_from_state(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"],
+                                           a["z"], a["bias"], a["softplus"], a["h0"], a["Bsz"],
+                                           a["Dch"], a["L"], a["N"], a["dtype"], a["y"],
+                                           a["h_last"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=7), DTYPE), (dict(N=32), NUNS), (dict(L=-1), SHAPE), (dict(u=None), NULL),
+    (dict(h0=MIS), ALIGN),
+])
+def test_fwd_from_state_rejects(kw, code):
+    assert fwd_from_state(**kw) == code
+
+
+def conv(**kw):
+    a = dict(x=P, w=P, bias=None, silu=1, Bsz=2, Dch=16, L=64, K=4, dtype=1, u=P)
+    a.update(kw)
+    return ss.lib().ss_conv1d_silu_fwd(a["x"], a["w"], a["bias"], a["silu"], a["Bsz"], a["Dch"],
+                                       a["L"], a["K"], a["dtype"], a["u"], None)
+
+
+def conv_bwd(**kw):
+    a = dict(x=P, w=P, bias=P, silu=1, du=P, Bsz=2, Dch=16, L=64, K=4, dtype=1, dx=P, dw=P,
+             dbias=P)
+    a.update(kw)
+    return ss.lib().ss_conv1d_silu_bwd(a["x"], a["w"], a["bias"], a["silu"], a["du"], a["Bsz"],
+                                       a["Dch"], a["L"], a["K"], a["dtype"], a["dx"], a["dw"],
+                                       a["dbias"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(K=0), SHAPE), (dict(K=5), SHAPE), (dict(L=-2), SHAPE), (dict(dtype=9), DTYPE),
+    (dict(x=None), NULL), (dict(w=None), NULL), (dict(u=None), NULL), (dict(x=MIS), ALIGN),
+    (dict(u=MIS), ALIGN),
+])
+def test_conv_rejects(kw, code):
+    assert conv(**kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(K=7), SHAPE), (dict(dtype=4), DTYPE), (dict(du=None), NULL), (dict(dw=None), NULL),
+    (dict(dbias=None), NULL), (dict(bias=None), NULL), (dict(dx=MIS), ALIGN),
+])
+def test_conv_bwd_rejects(kw, code):
+    assert conv_bwd(**kw) == code
+
+
+def test_conv_empty_forward_is_ok_without_pointers():
+    assert conv(x=None, w=None, u=None, L=0) == OK

@@ -40,6 +40,15 @@ MUTANTS = [
     ("step_B_for_C", "y += c->C[b * N + n] * *hn;", "y += c->B[b * N + n] * *hn;"),
     ("step_no_bias", "const double dt = softplus_or_raw(c->delta[row] + (c->bias ? c->bias[d] : 0.0), c->softplus);",
      "const double dt = softplus_or_raw(c->delta[row], c->softplus);"),
+    ("conv_taps_not_flipped", "if (src >= 0) s += c->w[d * c->K + k] * xr[src];",
+     "if (src >= 0) s += c->w[d * c->K + (c->K - 1 - k)] * xr[src];"),
+    ("conv_bias_dropped", "double s = c->bias ? c->bias[d] : 0.0;", "double s = 0.0;"),
+    ("conv_silu_derivative_wrong", "c->g[row * L + t] * s * (1.0 + v * (1.0 - s))",
+     "c->g[row * L + t] * s"),
+    ("conv_dx_wrong_tap", "if (t < L) acc += c->w[d * K + k] * gc[t];",
+     "if (t < L) acc += c->w[d * K + (K - 1 - k)] * gc[t];"),
+    ("conv_dw_wrong_shift", "if (src >= 0) c->dw[d * K + k] += gc[t] * xr[src];",
+     "if (src >= 1) c->dw[d * K + k] += gc[t] * xr[src - 1];"),
 ]
 
 
