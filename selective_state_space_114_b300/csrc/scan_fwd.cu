@@ -7,9 +7,12 @@
 // sequential loop of the "PyTorch 한 파일에서의 Mamba 구현" thread
 // (news.hada.io, topic 12448), evaluated here as a chunked parallel scan.
 //
-// Two kernels.  scan_fwd_pair_kernel (below) serves rows whose byte length
-// is a multiple of 16; scan_fwd_kernel, the element-wise version of the same
-// scheme, serves any other L.  Common scheme -- grid: x = channel groups of
+// Three kernels.  scan_fwd_rows_kernel (at the end) walks each row in time
+// order with the states split over a quad of lanes; it serves workloads with
+// many rows whose byte length is a multiple of 16.  The two chunked kernels
+// split the sequence of a row across lanes instead: scan_fwd_pair_kernel for
+// rows of 16-byte multiples, scan_fwd_kernel, the element-wise version of
+// the same scheme, for any other L.  Chunked scheme -- grid: x = channel groups of
 // R = 2W rows, y = batch.  Each warp holds two rows; the lanes of a row
 // split the current chunk into consecutive segments (see common.cuh).  The
 // CTA stages B and C of its batch for the chunk once in shared memory (as
@@ -280,6 +283,283 @@ __global__ void __launch_bounds__(W * 32)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Row-sequential kernel (rows whose length is a multiple of the 16-byte
+// vector, and enough rows to occupy every SM).
+//
+// The recurrence of a row is walked in time order by a quad of lanes, each
+// lane holding four of the sixteen states in registers for the whole
+// sequence, so every h_t is formed exactly once (the chunked kernels form it
+// twice: a fold of the chunk and a replay from the carried prefix).  A CTA
+// takes R rows of one batch through the sequence in tiles of T steps, three
+// phases per tile:
+//   A  element-parallel: delta -> dt = softplus(delta + bias) and dt*u into
+//      shared memory; B and C of the tile converted once to float [t][n]
+//      (all R rows share them);
+//   B  row quads: T steps of the recurrence; per step each lane adds the
+//      C.h terms of its four states and writes that partial to shared
+//      memory (four steps per 128-bit store);
+//   C  element-parallel: y = sum of the four partials + D u, times silu(z),
+//      stored as 16-byte vectors.
+// Phase C of a tile shares the barrier interval of the next tile's phase A.
+// B/C tiles arrive by cp.async one tile ahead; u and delta of the next tile
+// and z of the current one are loaded into registers during phase B.
+// Steps at or past L and rows past Dch get dt = 0 (the state stays put).
+// ---------------------------------------------------------------------------
+template <typename Io, int R, int T, int NR>
+struct FwdRowsCfg {
+  using E = typename Io::T;
+  static constexpr int NT = 4 * R / NR;          // threads: a quad per NR rows
+  static constexpr int V = Io::kVec;             // elements per 16-byte vector
+  static constexpr int VPR = T / V;              // vectors of a row in a tile
+  static constexpr int NV = R * VPR / NT;        // vectors per thread, phases A/C
+  static constexpr int RAWB = T * (int)sizeof(E) + 16;  // raw B/C row bytes (padded)
+  static constexpr int CF_OFF = 16 * T + 16;     // C tile offset from B tile (floats)
+  static constexpr int DDS = 2 * T + 4;          // (dt, dt*u) row stride (floats)
+  static constexpr int YPS = 4 * T + 16;         // partial row stride (floats)
+  static constexpr size_t raw_bytes = 2ull * 2 * kN * RAWB;
+  static constexpr size_t smem =
+      raw_bytes + sizeof(float) * ((size_t)CF_OFF + 16 * T + (size_t)R * DDS + (size_t)R * YPS);
+  static_assert(NV >= 1 && R * VPR == NV * NT, "whole vectors per thread");
+  static_assert(T % 4 == 0 && (RAWB % 16) == 0 && R % (8 * NR) == 0, "tile shape");
+};
+
+template <typename Io, int R, int T, int NR>
+__global__ void __launch_bounds__(4 * R / NR)
+    scan_fwd_rows_kernel(ScanArgs p, typename Io::T* __restrict__ y_out, float* __restrict__ h_last) {
+  using E = typename Io::T;
+  using Cfg = FwdRowsCfg<Io, R, T, NR>;
+  constexpr int NT = Cfg::NT, V = Cfg::V, VPR = Cfg::VPR, NV = Cfg::NV;
+  constexpr int RAWE = Cfg::RAWB / (int)sizeof(E);  // raw row stride in elements
+  extern __shared__ float4 smem4[];
+  char* base = reinterpret_cast<char*>(smem4);
+  E* raw = reinterpret_cast<E*>(base);  // [2 buffers][2 * kN rows][RAWE]
+  float* Bf = reinterpret_cast<float*>(base + Cfg::raw_bytes);
+  float* Cf = Bf + Cfg::CF_OFF;
+  float* dd = Cf + 16 * T;  // [R][DDS]
+  float* yp = dd + R * Cfg::DDS;  // [R][YPS]
+
+  const int tid = threadIdx.x;
+  const int64_t b = blockIdx.y, L = p.L, Dch = p.Dch;
+  const int64_t d0 = (int64_t)blockIdx.x * R;
+  const E* Bb = static_cast<const E*>(p.B) + b * kN * L;
+  const E* Cb = static_cast<const E*>(p.C) + b * kN * L;
+
+  // recurrence lane: rows qr + j R / NR (j < NR), states 4 qk .. 4 qk + 3
+  const int qr = tid >> 2, qk = tid & 3;
+  float2 A01[NR], A23[NR], h01[NR], h23[NR];
+#pragma unroll
+  for (int j = 0; j < NR; ++j) {
+    const int64_t qd = d0 + qr + j * (R / NR);
+    A01[j] = A23[j] = h01[j] = h23[j] = make_float2(0.f, 0.f);
+    if (qd < Dch) {
+      const float4 a = *reinterpret_cast<const float4*>(p.A + qd * kN + 4 * qk);
+      A01[j] = make_float2(a.x * kLog2e, a.y * kLog2e);
+      A23[j] = make_float2(a.z * kLog2e, a.w * kLog2e);
+      if (p.h0) {
+        const float4 h = *reinterpret_cast<const float4*>(p.h0 + ((b * Dch + qd) * kN + 4 * qk));
+        h01[j] = make_float2(h.x, h.y);
+        h23[j] = make_float2(h.z, h.w);
+      }
+    }
+  }
+
+  // element lanes: vector m covers row er[m], steps es[m] * V .. + V of a tile
+  int er[NV], es[NV];
+  bool ev[NV];
+  float ebias[NV], eD[NV];
+  const E* eu[NV];
+  const E* edl[NV];
+  const E* ez[NV];
+  E* ey[NV];
+#pragma unroll
+  for (int m = 0; m < NV; ++m) {
+    const int v = tid + NT * m;
+    er[m] = v / VPR;
+    es[m] = v % VPR;
+    const int64_t d = d0 + er[m];
+    ev[m] = d < Dch;
+    const int64_t row = b * Dch + (ev[m] ? d : 0);
+    ebias[m] = (ev[m] && p.delta_bias) ? p.delta_bias[d] : 0.f;
+    eD[m] = (ev[m] && p.D) ? p.D[d] : 0.f;
+    eu[m] = static_cast<const E*>(p.u) + row * L + es[m] * V;
+    edl[m] = static_cast<const E*>(p.delta) + row * L + es[m] * V;
+    ez[m] = p.z ? static_cast<const E*>(p.z) + row * L + es[m] * V : nullptr;
+    ey[m] = y_out + row * L + es[m] * V;
+  }
+  const uint4 zero4 = make_uint4(0, 0, 0, 0);
+
+  auto issue_bc = [&](int64_t t0, E* dst) {
+    for (int i = tid; i < 2 * kN * VPR; i += NT) {
+      const int rr = i / VPR, s = i % VPR;  // rr = w * kN + n
+      const E* src = (rr < kN ? Bb + (int64_t)rr * L : Cb + (int64_t)(rr - kN) * L);
+      const int64_t t = t0 + s * V;
+      const bool in = t < L;
+      cp_async16(dst + rr * RAWE + s * V, in ? (const void*)(src + t) : (const void*)src,
+                 in ? 16 : 0);
+    }
+  };
+
+  issue_bc(0, raw);
+  cp_async_commit();
+  uint4 ru[NV], rd[NV], rz[NV], ru_cur[NV];
+#pragma unroll
+  for (int m = 0; m < NV; ++m) {
+    const bool in = ev[m] && es[m] * V < L;
+    ru[m] = in ? ldg_nc_v4(eu[m]) : zero4;
+    rd[m] = in ? ldg_nc_v4(edl[m]) : zero4;
+    rz[m] = zero4;
+    ru_cur[m] = zero4;
+  }
+
+  for (int64_t t0 = 0, i = 0;; t0 += T, ++i) {
+    cp_async_wait_all();
+    __syncthreads();  // tile i's B/C landed; phase B of tile i-1 done
+
+    // ---- phase C of tile i-1
+    if (t0 > 0) {
+      const int64_t tp = t0 - T;
+#pragma unroll
+      for (int m = 0; m < NV; ++m) {
+        const int64_t t = tp + es[m] * V;
+        if (!ev[m] || t >= L) continue;
+        const int rot = (V == 8 ? es[m] : es[m] >> 1) & 3;  // bank-conflict-free order
+        const float4* prow = reinterpret_cast<const float4*>(yp + er[m] * Cfg::YPS);
+        float y[V], u[V];
+#pragma unroll
+        for (int h = 0; h < V / 4; ++h) {
+          const int g = es[m] * (V / 4) + h;
+          float2 lo = make_float2(0.f, 0.f), hi = lo;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const float4 q = prow[4 * g + ((kk + rot) & 3)];
+            lo = add2(lo, make_float2(q.x, q.y));
+            hi = add2(hi, make_float2(q.z, q.w));
+          }
+          y[4 * h] = lo.x;
+          y[4 * h + 1] = lo.y;
+          y[4 * h + 2] = hi.x;
+          y[4 * h + 3] = hi.y;
+        }
+        Io::unpack(ru_cur[m], u);
+#pragma unroll
+        for (int e = 0; e < V; ++e) y[e] = fmaf(eD[m], u[e], y[e]);
+        if (ez[m]) {
+          float zz[V];
+          Io::unpack(rz[m], zz);
+#pragma unroll
+          for (int e = 0; e < V; ++e) y[e] *= zz[e] * sigmoid_f(zz[e]);
+        }
+        stg_v4(ey[m] + tp, Io::pack(y));
+      }
+    }
+    if (t0 >= L) break;
+
+    // ---- phase A of tile i
+    {
+      const E* rb = raw + (i & 1) * (2 * kN * RAWE);
+      for (int it = tid; it < 2 * kN * VPR; it += NT) {
+        const int w = (it >> 4) & 1, n = it & 15, ts = it >> 5;
+        float f[V];
+        Io::unpack(*reinterpret_cast<const uint4*>(rb + (w * kN + n) * RAWE + ts * V), f);
+        float* X = w ? Cf : Bf;
+#pragma unroll
+        for (int e = 0; e < V; ++e) X[(ts * V + e) * kN + n] = f[e];
+      }
+    }
+    if (t0 + T < L) issue_bc(t0 + T, raw + ((i + 1) & 1) * (2 * kN * RAWE));
+    cp_async_commit();
+#pragma unroll
+    for (int m = 0; m < NV; ++m) {
+      const int64_t t = t0 + es[m] * V;
+      const bool in = ev[m] && t < L;
+      float u[V], dl[V];
+      Io::unpack(ru[m], u);
+      Io::unpack(rd[m], dl);
+      float q[2 * V];
+#pragma unroll
+      for (int e = 0; e < V; ++e) {
+        const float x = dl[e] + ebias[m];
+        float dt = p.softplus ? softplus_fast(x) : x;
+        dt = in ? dt : 0.f;
+        q[2 * e] = dt;
+        q[2 * e + 1] = dt * u[e];
+      }
+      float4* dst = reinterpret_cast<float4*>(dd + er[m] * Cfg::DDS + 2 * es[m] * V);
+#pragma unroll
+      for (int c = 0; c < V / 2; ++c)
+        dst[c] = make_float4(q[4 * c], q[4 * c + 1], q[4 * c + 2], q[4 * c + 3]);
+      // registers for phase C of this tile and phase A of the next one
+      ru_cur[m] = ru[m];
+      rz[m] = (in && ez[m]) ? ldg_nc_v4(ez[m] + t0) : zero4;
+      const bool nin = ev[m] && t + T < L;
+      ru[m] = nin ? ldg_nc_v4(eu[m] + t0 + T) : zero4;
+      rd[m] = nin ? ldg_nc_v4(edl[m] + t0 + T) : zero4;
+    }
+    __syncthreads();  // (dt, dt*u) and the B/C tile ready; phase C of tile i-1 done
+
+    // ---- phase B of tile i
+    {
+      const float4* B4 = reinterpret_cast<const float4*>(Bf) + qk;
+      const float4* C4 = reinterpret_cast<const float4*>(Cf) + qk;
+#pragma unroll 2
+      for (int g = 0; g < T / 4; ++g) {
+        float dts[NR][4], dus[NR][4], yv[NR][4];
+#pragma unroll
+        for (int j = 0; j < NR; ++j) {
+          const float4* d4 = reinterpret_cast<const float4*>(dd + (qr + j * (R / NR)) * Cfg::DDS);
+          const float4 q0 = d4[2 * g], q1 = d4[2 * g + 1];
+          dts[j][0] = q0.x, dts[j][1] = q0.z, dts[j][2] = q1.x, dts[j][3] = q1.z;
+          dus[j][0] = q0.y, dus[j][1] = q0.w, dus[j][2] = q1.y, dus[j][3] = q1.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = 4 * g + e;
+          const float4 bv = B4[4 * t], cv = C4[4 * t];
+#pragma unroll
+          for (int j = 0; j < NR; ++j) {
+            const float2 dt2 = make_float2(dts[j][e], dts[j][e]);
+            const float2 e01 = mul2(dt2, A01[j]), e23 = mul2(dt2, A23[j]);
+            const float2 a01 = make_float2(ex2f(e01.x), ex2f(e01.y));
+            const float2 a23 = make_float2(ex2f(e23.x), ex2f(e23.y));
+            const float2 du2 = make_float2(dus[j][e], dus[j][e]);
+            h01[j] = fma2(a01, h01[j], mul2(du2, make_float2(bv.x, bv.y)));
+            h23[j] = fma2(a23, h23[j], mul2(du2, make_float2(bv.z, bv.w)));
+            const float2 yy =
+                fma2(make_float2(cv.z, cv.w), h23[j], mul2(make_float2(cv.x, cv.y), h01[j]));
+            yv[j][e] = yy.x + yy.y;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < NR; ++j)
+          reinterpret_cast<float4*>(yp + (qr + j * (R / NR)) * Cfg::YPS)[4 * g + qk] =
+              make_float4(yv[j][0], yv[j][1], yv[j][2], yv[j][3]);
+      }
+    }
+  }
+  if (h_last) {
+#pragma unroll
+    for (int j = 0; j < NR; ++j) {
+      const int64_t qd = d0 + qr + j * (R / NR);
+      if (qd < Dch)
+        *reinterpret_cast<float4*>(h_last + (b * Dch + qd) * kN + 4 * qk) =
+            make_float4(h01[j].x, h01[j].y, h23[j].x, h23[j].y);
+    }
+  }
+}
+
+template <typename Io, int R, int T, int NR>
+static cudaError_t launch_fwd_rows(const ScanArgs& a, void* y, float* h_last, cudaStream_t s) {
+  using Cfg = FwdRowsCfg<Io, R, T, NR>;
+  auto kern = scan_fwd_rows_kernel<Io, R, T, NR>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((a.Dch + R - 1) / R), (unsigned)a.Bsz);
+  kern<<<grid, Cfg::NT, Cfg::smem, s>>>(a, static_cast<typename Io::T*>(y), h_last);
+  return cudaGetLastError();
+}
+
 template <typename Io, int W, int KT>
 static cudaError_t launch_fwd_pair(const ScanArgs& a, void* y, float* h_last, cudaStream_t s) {
   using Cfg = FwdPairCfg<Io, W, KT>;
@@ -304,20 +584,32 @@ static cudaError_t launch_fwd_t(const ScanArgs& a, void* y, float* h_last, cudaS
   return cudaGetLastError();
 }
 
-// Rows of 16-byte multiples take the paired kernel in the configuration that
-// measured fastest for the I/O type (bf16 8 x 1536 x 2048: 4 warps, 16 steps
-// per lane, also used for fp16; fp32 8 x 2048 x 2048: 8 warps, 8 steps per
-// lane); other lengths the element-wise kernel.
+// Rows of 16-byte multiples: with at least 8192 rows (enough quads of lanes to
+// occupy every SM) the row-sequential kernel, 32 channels per CTA, one row
+// per quad for 16-bit I/O and two for fp32 (measured fastest: bf16 8 x 1536
+// x 2048, fp32 8 x 2048 x 2048); with fewer rows the chunked paired kernel
+// (bf16 / fp16: 4 warps, 16 steps per lane; fp32: 8 warps, 8 steps per
+// lane), which splits the sequence across lanes.  Other lengths take the
+// element-wise kernel.
+constexpr int64_t kRowsKernelMinRows = 8192;
+
 cudaError_t launch_scan_fwd(const ScanArgs& a, void* y, float* h_last, cudaStream_t s) {
+  const bool many_rows = a.Bsz * a.Dch >= kRowsKernelMinRows;
   if (a.dt == Dt::BF16) {
-    if (a.L % IoBf16::kVec == 0) return launch_fwd_pair<IoBf16, 4, 16>(a, y, h_last, s);
+    if (a.L % IoBf16::kVec == 0)
+      return many_rows ? launch_fwd_rows<IoBf16, 32, 32, 1>(a, y, h_last, s)
+                       : launch_fwd_pair<IoBf16, 4, 16>(a, y, h_last, s);
     return launch_fwd_t<IoBf16, 8, false>(a, y, h_last, s);
   }
   if (a.dt == Dt::F16) {
-    if (a.L % IoF16::kVec == 0) return launch_fwd_pair<IoF16, 4, 16>(a, y, h_last, s);
+    if (a.L % IoF16::kVec == 0)
+      return many_rows ? launch_fwd_rows<IoF16, 32, 32, 1>(a, y, h_last, s)
+                       : launch_fwd_pair<IoF16, 4, 16>(a, y, h_last, s);
     return launch_fwd_t<IoF16, 8, false>(a, y, h_last, s);
   }
-  if (a.L % IoF32::kVec == 0) return launch_fwd_pair<IoF32, 8, 8>(a, y, h_last, s);
+  if (a.L % IoF32::kVec == 0)
+    return many_rows ? launch_fwd_rows<IoF32, 32, 32, 2>(a, y, h_last, s)
+                     : launch_fwd_pair<IoF32, 8, 8>(a, y, h_last, s);
   return launch_fwd_t<IoF32, 8, false>(a, y, h_last, s);
 }
 

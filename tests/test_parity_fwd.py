@@ -234,3 +234,62 @@ def test_from_state_empty_sequence_copies_the_state():
     _, hl = ss.ss_scan_fwd(u, u, A, B, B, return_last_state=True, h0=h0)
     torch.cuda.synchronize()
     assert torch.equal(hl, h0)
+
+
+# --- the row-sequential kernel: rows (Bsz * Dch) >= 8192 with L a multiple of
+# the 16-byte vector select it; tiles are 32 steps, CTAs 32 channels.
+ROWS_SHAPES = [
+    (4, 2080, 200),  # channels not a multiple of the CTA, a ragged last tile
+    (8, 1040, 32),   # exactly one tile
+    (2, 4100, 8),    # less than one tile
+    (1, 8200, 72),   # one batch, two full tiles and a part
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("Bsz,Dch,L", ROWS_SHAPES)
+def test_rows_kernel_shapes(dtype, Bsz, Dch, L):
+    x = make_case(dtype, Bsz, Dch, L, seed=300 + L + Dch)
+    compare(x, dtype, what=f"rows {dtype} {Bsz}x{Dch}x{L}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("drop", ["D", "z", "delta_bias", "all", "softplus"])
+def test_rows_kernel_optional_inputs(dtype, drop):
+    x = make_case(dtype, 4, 2060, 96, seed=17)
+    softplus = True
+    if drop == "all":
+        x.update(D=None, z=None, delta_bias=None)
+    elif drop == "softplus":
+        softplus = False
+        x["delta"] = as_io(np.abs(synth.widen(x["delta"])) * 0.05, dtype)
+        x["delta_bias"] = np.zeros_like(x["delta_bias"])
+    else:
+        x[drop] = None
+    compare(x, dtype, softplus=softplus, what=f"rows {dtype} drop={drop}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_rows_kernel_from_state_in_place(dtype):
+    """Row-sequential kernel continued from a state updated in place."""
+    Bsz, Dch, L = 4, 2070, 136
+    x = make_case(dtype, Bsz, Dch, L, seed=71)
+    h0 = np.random.default_rng(9).standard_normal((Bsz, Dch, 16)).astype(np.float32)
+    xd = inputs_to_dev(x, dtype)
+    h = torch.from_numpy(h0).cuda()
+    y, hl = ss.ss_scan_fwd(xd["u"], xd["delta"], xd["A"], xd["B"], xd["C"], xd["D"], xd["z"],
+                           xd["delta_bias"], True, return_last_state=True, h0=h, h_last=h)
+    torch.cuda.synchronize()
+    assert hl.data_ptr() == h.data_ptr()
+    ref, href = oracle_fwd(x, True, h0=h0.astype(np.float64))
+    check(to_host64(y), ref, out_kind(dtype), f"rows {dtype} from state y")
+    check(to_host64(hl), href, "f32" if dtype == "f32" else out_kind(dtype), "rows h_last")
+
+
+def test_rows_kernel_deterministic():
+    x = make_case("bf16", 4, 2048, 160, seed=12)
+    xd = inputs_to_dev(x, "bf16")
+    y1, h1 = run_fwd(xd)
+    y2, h2 = run_fwd(xd)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2) and torch.equal(h1, h2)
