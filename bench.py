@@ -465,6 +465,138 @@ def decode_step_measure(ss, dev, seed, steps=16):
             "frac": round(ach / hbm, 4), "algorithmic_bytes": nbytes}
 
 
+def _device_inputs(cfg, dev, seed, with_dy=False):
+    """Inputs of a workload made on the device: activations and B/C drawn from
+    N(0, 1) by torch's seeded generator (the workload's distributions, not the
+    host generator's values; timing does not depend on them), A, D and
+    delta_bias from the host generator."""
+    import torch
+    Bsz, Dch, L, N = cfg["Bsz"], cfg["Dch"], cfg["L"], cfg["N"]
+    dtype = torch.bfloat16 if cfg["dtype"] == "bf16" else torch.float32
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+
+    def rnd(*shape):
+        return torch.randn(shape, generator=gen, device=dev, dtype=torch.float32).to(dtype)
+
+    x = {"u": rnd(Bsz, Dch, L), "delta": rnd(Bsz, Dch, L), "z": rnd(Bsz, Dch, L),
+         "B": rnd(Bsz, N, L), "C": rnd(Bsz, N, L)}
+    if with_dy:
+        x["dy"] = rnd(Bsz, Dch, L)
+    x["A"] = torch.from_numpy(synth.param_A(Dch, N)).to(dev)
+    x["D"] = torch.from_numpy(synth.param_D(seed, Dch)).to(dev)
+    x["delta_bias"] = torch.from_numpy(synth.param_delta_bias(seed, Dch, cfg["dt_range"])).to(dev)
+    return x, dtype
+
+
+def _timed_ms(fns, steps, dev):
+    """Mean device time of each function in fns over `steps` back-to-back
+    rounds (inputs far larger than L2, so no flush), after 3 warm-up rounds."""
+    import torch
+    for _ in range(3):
+        for f in fns:
+            f()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)]
+           for _ in range(steps)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(50_000_000)
+    for row in evs:
+        row[0].record()
+        for i, f in enumerate(fns):
+            f()
+            row[i + 1].record()
+    torch.cuda.synchronize()
+    return [statistics.mean(r[i].elapsed_time(r[i + 1]) for r in evs) for i in range(len(fns))]
+
+
+def configs_measure(ss, dev, seed):
+    """The other full-size workloads: the fp32 Mamba-370M-shaped layer forward
+    and backward (8 x 2048 x 2048) and the long-sequence bf16 forward
+    (1 x 5120 x 131072), each kernel stage with its roofline."""
+    import torch
+    hbm, _ = load_peaks()
+    out = {}
+    cfg = synth.config(2)
+    x, dtype = _device_inputs(cfg, dev, seed + 2, with_dy=True)
+    Bsz, Dch, L, N = cfg["Bsz"], cfg["Dch"], cfg["L"], cfg["N"]
+    E = Bsz * Dch * L
+    y = torch.empty_like(x["u"])
+    g = {"du": torch.empty_like(y), "ddelta": torch.empty_like(y), "dz": torch.empty_like(y),
+         "dA": torch.empty((Dch, N), device=dev), "dB": torch.empty((Bsz, N, L), device=dev),
+         "dC": torch.empty((Bsz, N, L), device=dev), "dD": torch.empty((Dch,), device=dev),
+         "ddelta_bias": torch.empty((Dch,), device=dev)}
+    ws = torch.empty(ss.ss_scan_bwd_workspace_size(Bsz, Dch, L, N, ss.SS_F32), device=dev,
+                     dtype=torch.uint8)
+    args = (x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], True)
+    fns = [lambda: ss.ss_scan_fwd(*args, out=y)]
+    names = ["fwd", "bwd_states", "bwd_reverse", "bwd_reduce"]
+    for st in ("ss_scan_bwd_states", "ss_scan_bwd_reverse", "ss_scan_bwd_reduce"):
+        fns.append(lambda st=st: ss.ss_scan_bwd(*args, x["dy"], workspace=ws, out=g,
+                                                stages=(st,)))
+    ms = _timed_ms(fns, 10, dev)
+    work = kernel_work(4, Dch)
+    tot = sum(ms)
+    out["mamba370m_fp32_fwd_bwd"] = {
+        "workload": f"Bsz={Bsz} Dch={Dch} L={L} N={N}, fp32 I/O, fwd + bwd, inputs larger than L2",
+        "gelem_s": round(E / (tot * 1e-3) / 1e9, 3), "ms": round(tot, 4),
+        "kernels": {nm: {"ms": round(t, 4), **{k: v for k, v in roofline(nm, work[nm], E, t, hbm)
+                                               .items() if k in ("bound", "achieved", "peak",
+                                                                 "unit", "frac", "resource")}}
+                    for nm, t in zip(names, ms)}}
+    del x, y, g, ws
+    torch.cuda.empty_cache()
+
+    cfg = synth.config(3)
+    x, dtype = _device_inputs(cfg, dev, seed + 3)
+    Bsz, Dch, L, N = cfg["Bsz"], cfg["Dch"], cfg["L"], cfg["N"]
+    E = Bsz * Dch * L
+    y = torch.empty_like(x["u"])
+    h = torch.empty((Bsz, Dch, N), device=dev)
+    args = (x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], True)
+    (t,) = _timed_ms([lambda: ss.ss_scan_fwd(*args, out=y, h_last=h, return_last_state=True)],
+                     5, dev)
+    r = roofline("fwd", kernel_work(2, Dch)["fwd"], E, t, hbm)
+    out["long_sequence_bf16_fwd"] = {
+        "workload": f"Bsz={Bsz} Dch={Dch} L={L} N={N}, bf16 I/O, f32 state, fwd, "
+                    f"inputs larger than L2",
+        "gelem_s": round(E / (t * 1e-3) / 1e9, 3), "ms": round(t, 4),
+        **{k: v for k, v in r.items() if k in ("bound", "achieved", "peak", "unit", "frac",
+                                               "resource")}}
+    del x, y, h
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_profile_workload(args):
+    """Run a workload's kernels `--profile-iters` times and exit, for an ncu
+    capture of one launch: mamba370m (the fp32 8 x 2048 x 2048 layer, forward
+    then backward) or long_sequence (the bf16 1 x 5120 x 131072 forward; the
+    length may be cut with --profile-L to keep a capture small)."""
+    import torch
+    import selective_state_space_114_b300 as ss
+    dev = torch.device("cuda", 0)
+    ci = {"mamba370m": 2, "long_sequence": 3}[args.profile_workload]
+    cfg = synth.config(ci)
+    if args.profile_L:
+        cfg = dict(cfg, L=args.profile_L)
+    x, _ = _device_inputs(cfg, dev, cfg["seed"], with_dy=(ci == 2))
+    Bsz, Dch, L, N = cfg["Bsz"], cfg["Dch"], cfg["L"], cfg["N"]
+    args_ = (x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], True)
+    y = torch.empty_like(x["u"])
+    ws = None
+    if ci == 2:
+        ws = torch.empty(ss.ss_scan_bwd_workspace_size(Bsz, Dch, L, N, ss.SS_F32), device=dev,
+                         dtype=torch.uint8)
+    for _ in range(args.profile_iters):
+        ss.ss_scan_fwd(*args_, out=y)
+        if ws is not None:
+            ss.ss_scan_bwd(*args_, x["dy"], workspace=ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_workload": args.profile_workload, "Bsz": Bsz, "Dch": Dch, "L": L,
+                      "iters": args.profile_iters}))
+    return 0
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -560,6 +692,7 @@ def run_ours(args):
 
     decode = decode_step_measure(ss, dev, seed) if rank == 0 else None
     conv = conv_measure(ss, dev, seed) if rank == 0 else None
+    others = configs_measure(ss, dev, seed) if rank == 0 else None
 
     # end to end through the public API with host buffers
     Ke = max(3, min(K, 10))
@@ -606,6 +739,7 @@ def run_ours(args):
         "gpu_launches": K * LAUNCHES_PER_STEP,
         "decode_step": decode,
         "conv1d_silu": conv,
+        "other_workloads": others,
         "e2e": {"value": round(world * E / (e2e_ms * 1e-3) / 1e9, 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 3)},
@@ -627,7 +761,13 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing on the host cores")
+    ap.add_argument("--profile-workload", choices=["mamba370m", "long_sequence"],
+                    help="only run that workload's kernels (for an ncu capture) and exit")
+    ap.add_argument("--profile-L", type=int, default=0)
+    ap.add_argument("--profile-iters", type=int, default=2)
     args = ap.parse_args()
+    if args.profile_workload:
+        return run_profile_workload(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
