@@ -43,6 +43,8 @@
  *     execution surface at the caller's next synchronisation.
  *   - Outputs are overwritten, never accumulated into.
  *   - N (the state size, d_state) must be 16.
+ *   - Bsz is at most 65535 for the scan and step entry points (SS_ERR_SHAPE
+ *     otherwise): the batch index is a grid dimension.
  */
 #ifndef SELSCAN_H_
 #define SELSCAN_H_

@@ -214,7 +214,7 @@ ss_status ss_step(float* h, const void* u_t, const void* delta_t, const float* A
                   ss_dtype dtype, void* y_t, ss_stream_t stream) {
   if (!known_dtype(dtype)) return SS_ERR_DTYPE;
   if (bad_size(Bsz) || bad_size(Dch) || bad_size(N)) return SS_ERR_SHAPE;
-  if (product_too_big(Bsz, Dch, 4)) return SS_ERR_SHAPE;
+  if (Bsz > 65535 || product_too_big(Bsz, Dch, 4)) return SS_ERR_SHAPE;
   if (N != 16) return SS_ERR_N_UNSUPPORTED;
   if (Bsz == 0 || Dch == 0) return SS_OK;
   if (!h || !u_t || !delta_t || !A || !B_t || !C_t || !y_t) return SS_ERR_NULL;

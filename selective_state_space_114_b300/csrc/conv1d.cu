@@ -16,6 +16,7 @@ namespace selscan {
 namespace {
 
 constexpr int kConvThreads = 256;
+constexpr int kConvBwdRun = 2;  // consecutive vectors per backward item
 
 // silu'(c) = s (1 + c (1 - s)), s = sigmoid(c)
 __device__ __forceinline__ float silu_grad(float c) {
@@ -94,60 +95,77 @@ __global__ void __launch_bounds__(kConvThreads, 4) conv_bwd_kernel(ConvArgs p, C
   float dw[K], db = 0.f;
 #pragma unroll
   for (int k = 0; k < K; ++k) dw[k] = 0.f;
-  const int64_t vecs = (L + V - 1) / V;
-  const int64_t items = p.Bsz * vecs;  // (batch, vector) pairs of this channel
+  // items: (batch, run of kConvBwdRun consecutive vectors) of this channel;
+  // a run loads its K-1 halo steps on each side once
+  constexpr int S = kConvBwdRun * V;  // steps per item
+  const int64_t runs = (L + S - 1) / S;
+  const int64_t items = p.Bsz * runs;
+  // the item index it = b * runs + v advances by kConvThreads per pass: keep
+  // (b, v) incrementally instead of dividing every pass
+  int64_t b = tid / runs, v = tid - (tid / runs) * runs;
+  const int64_t bstep = kConvThreads / runs, vstep = kConvThreads - bstep * runs;
   for (int64_t it = tid; it < items; it += kConvThreads) {
-    const int64_t b = it / vecs, t0 = (it - b * vecs) * V;
+    const int64_t t0 = v * S;
     const int64_t row = b * p.Dch + d;
     const T* xr = static_cast<const T*>(p.x) + row * L;
     const T* gr = static_cast<const T*>(o.g) + row * L;
-    // x_{t0-(K-1)} .. x_{t0+V-1+(K-1)} and g_{t0} .. g_{t0+V-1+(K-1)}
-    float xx[V + 2 * (K - 1)], gg[V + K - 1];
+    v += vstep;
+    b += bstep;
+    if (v >= runs) {
+      v -= runs;
+      ++b;
+    }
+    // x_{t0-(K-1)} .. x_{t0+S-1+(K-1)} and g_{t0} .. g_{t0+S-1+(K-1)}; the
+    // loads give 0 at and past L, so gc = 0 there and no step past L adds
+    // to dw, dbias or dx
+    float xx[S + 2 * (K - 1)], gg[S + K - 1];
     {
-      float prev[V], cur[V], next[V], gcur[V], gnext[V];
-      load_kt<Io, V, kVec>(xr, t0, L, true, cur);
-      load_kt<Io, V, kVec>(gr, t0, L, true, gcur);
+      float prev[V], cur[S], next[V], gcur[S], gnext[V];
+#pragma unroll
+      for (int r = 0; r < kConvBwdRun; ++r) {
+        float* c = cur + r * V;
+        float* gc_ = gcur + r * V;
+        load_kt<Io, V, kVec>(xr, t0 + r * V, L, true, *reinterpret_cast<float(*)[V]>(c));
+        load_kt<Io, V, kVec>(gr, t0 + r * V, L, true, *reinterpret_cast<float(*)[V]>(gc_));
+      }
       if (K > 1) {
         load_kt<Io, V, kVec>(xr, t0 - V, L, t0 > 0, prev);
-        load_kt<Io, V, kVec>(xr, t0 + V, L, true, next);
-        load_kt<Io, V, kVec>(gr, t0 + V, L, true, gnext);
+        load_kt<Io, V, kVec>(xr, t0 + S, L, true, next);
+        load_kt<Io, V, kVec>(gr, t0 + S, L, true, gnext);
       }
 #pragma unroll
       for (int q = 0; q < K - 1; ++q) {
         xx[q] = prev[V - (K - 1) + q];
-        xx[K - 1 + V + q] = next[q];
-        gg[V + q] = gnext[q];
+        xx[K - 1 + S + q] = next[q];
+        gg[S + q] = gnext[q];
       }
 #pragma unroll
-      for (int q = 0; q < V; ++q) {
+      for (int q = 0; q < S; ++q) {
         xx[K - 1 + q] = cur[q];
         gg[q] = gcur[q];
       }
     }
-    // gc_t for t = t0 .. t0+V-1+(K-1) (zero past L)
-    float gc[V + K - 1];
+    // gc_t for t = t0 .. t0+S-1+(K-1)
+    float gc[S + K - 1];
 #pragma unroll
-    for (int q = 0; q < V + K - 1; ++q) {
+    for (int q = 0; q < S + K - 1; ++q) {
       float c = bias;
 #pragma unroll
       for (int k = 0; k < K; ++k) c = fmaf(w[k], xx[q + k], c);
-      const float gq = (t0 + q < L) ? gg[q] : 0.f;
-      gc[q] = p.silu ? gq * silu_grad(c) : gq;
+      gc[q] = p.silu ? gg[q] * silu_grad(c) : gg[q];
     }
-    float dx[V];
+    float dx[S];
 #pragma unroll
-    for (int q = 0; q < V; ++q) {
+    for (int q = 0; q < S; ++q) {
       float acc = 0.f;
 #pragma unroll
       for (int k = 0; k < K; ++k) acc = fmaf(w[k], gc[q + (K - 1) - k], acc);
       dx[q] = acc;
-      if (t0 + q < L) {
-        db += gc[q];
+      db += gc[q];
 #pragma unroll
-        for (int k = 0; k < K; ++k) dw[k] = fmaf(gc[q], xx[q + k], dw[k]);
-      }
+      for (int k = 0; k < K; ++k) dw[k] = fmaf(gc[q], xx[q + k], dw[k]);
     }
-    store_kt<Io, V, kVec>(static_cast<T*>(o.dx) + row * L, t0, L, true, dx);
+    store_kt<Io, S, kVec>(static_cast<T*>(o.dx) + row * L, t0, L, true, dx);
   }
 #pragma unroll
   for (int k = 0; k < K; ++k) red[k][tid] = dw[k];

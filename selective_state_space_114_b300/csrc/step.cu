@@ -31,58 +31,78 @@ __device__ __forceinline__ void load4(const typename Io::T* p, float (&v)[4]) {
   }
 }
 
-template <typename Io>
-__global__ void __launch_bounds__(256) step_kernel(StepArgs p) {
-  using T = typename Io::T;
-  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t rows = p.Bsz * p.Dch;
-  const int64_t row = gid >> 2;
-  const int q = threadIdx.x & 3;  // states 4q .. 4q+3
-  const bool valid = row < rows;
-  const int64_t rr = valid ? row : 0;
-  const int64_t b = rr / p.Dch, d = rr % p.Dch;
+// Grid: x = blocks of kStepRowsPerCta channels, y = batch.  Quad qi of a CTA
+// owns channels d0 + qi + 64 m (m < kStepRowsPerThread): each of its loads and
+// stores of h covers 64 consecutive channels (4 KB) per CTA, every thread
+// keeps kStepRowsPerThread 16-byte state loads in flight, and the batch index
+// comes from the grid (no division).
+constexpr int kStepThreads = 256;
+constexpr int kStepRowsPerThread = 1;
+constexpr int kStepRowsPerCta = kStepThreads / 4 * kStepRowsPerThread;
 
-  float yp = 0.f, uu = 0.f, zz = 0.f;
-  float4 hv = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (valid) {
-    uu = Io::to_f(static_cast<const T*>(p.u)[rr]);
-    const float x = Io::to_f(static_cast<const T*>(p.delta)[rr]) +
-                    (p.delta_bias ? p.delta_bias[d] : 0.f);
-    const float dt = p.softplus ? softplus_fast(x) : x;
-    const float4 Av = *reinterpret_cast<const float4*>(p.A + d * kN + 4 * q);
-    float Bv[4], Cv[4];
-    load4<Io>(static_cast<const T*>(p.B) + b * kN + 4 * q, Bv);
-    load4<Io>(static_cast<const T*>(p.C) + b * kN + 4 * q, Cv);
-    hv = *reinterpret_cast<const float4*>(p.h + rr * kN + 4 * q);
-    const float dtu = dt * uu;
-    hv.x = fmaf(ex2f(dt * Av.x * kLog2e), hv.x, dtu * Bv[0]);
-    hv.y = fmaf(ex2f(dt * Av.y * kLog2e), hv.y, dtu * Bv[1]);
-    hv.z = fmaf(ex2f(dt * Av.z * kLog2e), hv.z, dtu * Bv[2]);
-    hv.w = fmaf(ex2f(dt * Av.w * kLog2e), hv.w, dtu * Bv[3]);
-    *reinterpret_cast<float4*>(p.h + rr * kN + 4 * q) = hv;
-    yp = fmaf(Cv[0], hv.x, fmaf(Cv[1], hv.y, fmaf(Cv[2], hv.z, Cv[3] * hv.w)));
-    if (p.z) zz = Io::to_f(static_cast<const T*>(p.z)[rr]);
+template <typename Io>
+__global__ void __launch_bounds__(kStepThreads) step_kernel(StepArgs p) {
+  using T = typename Io::T;
+  constexpr int M = kStepRowsPerThread;
+  const int q = threadIdx.x & 3;  // states 4q .. 4q+3
+  const int qi = threadIdx.x >> 2;
+  const int64_t b = blockIdx.y;
+  const int64_t d0 = (int64_t)blockIdx.x * kStepRowsPerCta + qi;
+
+  float Bv[4], Cv[4];
+  load4<Io>(static_cast<const T*>(p.B) + b * kN + 4 * q, Bv);
+  load4<Io>(static_cast<const T*>(p.C) + b * kN + 4 * q, Cv);
+  float4 hv[M], Av[M];
+  float uu[M], xx[M], zz[M];
+  bool valid[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    const int64_t d = d0 + 64 * m;
+    valid[m] = d < p.Dch;
+    const int64_t rr = b * p.Dch + (valid[m] ? d : 0);
+    hv[m] = valid[m] ? *reinterpret_cast<const float4*>(p.h + rr * kN + 4 * q)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    Av[m] = valid[m] ? *reinterpret_cast<const float4*>(p.A + d * kN + 4 * q)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    uu[m] = valid[m] ? Io::to_f(static_cast<const T*>(p.u)[rr]) : 0.f;
+    xx[m] = valid[m] ? Io::to_f(static_cast<const T*>(p.delta)[rr]) +
+                           (p.delta_bias ? p.delta_bias[d] : 0.f)
+                     : 0.f;
+    zz[m] = (valid[m] && p.z) ? Io::to_f(static_cast<const T*>(p.z)[rr]) : 0.f;
   }
-  yp += __shfl_xor_sync(0xffffffffu, yp, 1);
-  yp += __shfl_xor_sync(0xffffffffu, yp, 2);
-  if (valid && q == 0) {
-    float y = fmaf(p.D ? p.D[d] : 0.f, uu, yp);
-    if (p.z) y *= zz * sigmoid_f(zz);
-    static_cast<T*>(p.y)[rr] = Io::from_f(y);
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    const int64_t d = d0 + 64 * m;
+    const int64_t rr = b * p.Dch + (valid[m] ? d : 0);
+    const float dt = p.softplus ? softplus_fast(xx[m]) : xx[m];
+    const float dtu = dt * uu[m];
+    float4 h = hv[m];
+    h.x = fmaf(ex2f(dt * Av[m].x * kLog2e), h.x, dtu * Bv[0]);
+    h.y = fmaf(ex2f(dt * Av[m].y * kLog2e), h.y, dtu * Bv[1]);
+    h.z = fmaf(ex2f(dt * Av[m].z * kLog2e), h.z, dtu * Bv[2]);
+    h.w = fmaf(ex2f(dt * Av[m].w * kLog2e), h.w, dtu * Bv[3]);
+    if (valid[m]) *reinterpret_cast<float4*>(p.h + rr * kN + 4 * q) = h;
+    float yp = fmaf(Cv[0], h.x, fmaf(Cv[1], h.y, fmaf(Cv[2], h.z, Cv[3] * h.w)));
+    yp += __shfl_xor_sync(0xffffffffu, yp, 1);
+    yp += __shfl_xor_sync(0xffffffffu, yp, 2);
+    if (valid[m] && q == 0) {
+      float y = fmaf(p.D ? p.D[d] : 0.f, uu[m], yp);
+      if (p.z) y *= zz[m] * sigmoid_f(zz[m]);
+      static_cast<T*>(p.y)[rr] = Io::from_f(y);
+    }
   }
 }
 
 }  // namespace
 
 cudaError_t launch_step(const StepArgs& a, cudaStream_t s) {
-  const int64_t threads = a.Bsz * a.Dch * 4;
-  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  const dim3 grid((unsigned)((a.Dch + kStepRowsPerCta - 1) / kStepRowsPerCta), (unsigned)a.Bsz);
   if (a.dt == Dt::BF16)
-    step_kernel<IoBf16><<<blocks, 256, 0, s>>>(a);
+    step_kernel<IoBf16><<<grid, kStepThreads, 0, s>>>(a);
   else if (a.dt == Dt::F16)
-    step_kernel<IoF16><<<blocks, 256, 0, s>>>(a);
+    step_kernel<IoF16><<<grid, kStepThreads, 0, s>>>(a);
   else
-    step_kernel<IoF32><<<blocks, 256, 0, s>>>(a);
+    step_kernel<IoF32><<<grid, kStepThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

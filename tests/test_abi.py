@@ -133,6 +133,7 @@ def step(**kw):
     (dict(dtype=3), DTYPE),
     (dict(N=64), NUNS),
     (dict(Dch=-1), SHAPE),
+    (dict(Bsz=65536), SHAPE),
     (dict(h=None), NULL),
     (dict(y=None), NULL),
     (dict(h=MIS), ALIGN),
