@@ -42,7 +42,9 @@
  *     a launch error (cudaGetLastError after the launch); faults during
  *     execution surface at the caller's next synchronisation.
  *   - Outputs are overwritten, never accumulated into.
- *   - N (the state size, d_state) must be 16.
+ *   - N (the state size, d_state) is 16 for every entry point; the forward
+ *     scans and the step also take 8, 32 and 64 (SS_ERR_N_UNSUPPORTED
+ *     otherwise).  N = 16 is the tuned configuration.
  *   - Bsz is at most 65535 for the scan and step entry points (SS_ERR_SHAPE
  *     otherwise): the batch index is a grid dimension.
  */
@@ -68,7 +70,7 @@ typedef enum {
     SS_ERR_NULL = 1,           /* a required pointer is NULL                      */
     SS_ERR_SHAPE = 2,          /* negative or too-large size                      */
     SS_ERR_DTYPE = 3,          /* unknown ss_dtype                                */
-    SS_ERR_N_UNSUPPORTED = 4,  /* N != 16                                         */
+    SS_ERR_N_UNSUPPORTED = 4,  /* N not supported by the entry point (see above)  */
     SS_ERR_ALIGN = 5,          /* a pointer is not 16-byte aligned                */
     SS_ERR_WORKSPACE = 6,      /* workspace NULL/misaligned or smaller than needed */
     SS_ERR_CUDA = 7,           /* the CUDA runtime reported a launch error        */

@@ -29,6 +29,9 @@ bool known_dtype(ss_dtype d) { return d == SS_F32 || d == SS_BF16 || d == SS_F16
 
 Dt to_dt(ss_dtype d) { return d == SS_BF16 ? Dt::BF16 : d == SS_F16 ? Dt::F16 : Dt::F32; }
 
+// State sizes of the forward scans and the step (the backward takes 16 only).
+bool fwd_n_ok(int64_t N) { return N == 8 || N == 16 || N == 32 || N == 64; }
+
 }  // namespace
 
 extern "C" {
@@ -39,7 +42,8 @@ const char* ss_status_str(ss_status s) {
     case SS_ERR_NULL: return "SS_ERR_NULL: a required pointer is NULL";
     case SS_ERR_SHAPE: return "SS_ERR_SHAPE: a size is negative or too large";
     case SS_ERR_DTYPE: return "SS_ERR_DTYPE: unknown dtype";
-    case SS_ERR_N_UNSUPPORTED: return "SS_ERR_N_UNSUPPORTED: N must be 16";
+    case SS_ERR_N_UNSUPPORTED:
+      return "SS_ERR_N_UNSUPPORTED: N must be 16 (the forward scans and the step also take 8, 32, 64)";
     case SS_ERR_ALIGN: return "SS_ERR_ALIGN: a pointer is not 16-byte aligned";
     case SS_ERR_WORKSPACE: return "SS_ERR_WORKSPACE: workspace missing, misaligned or too small";
     case SS_ERR_CUDA: return "SS_ERR_CUDA: the CUDA runtime reported an error";
@@ -61,7 +65,7 @@ ss_status run_fwd(const void* u, const void* delta, const float* A, const void* 
   if (!known_dtype(dtype)) return SS_ERR_DTYPE;
   if (bad_size(Bsz) || bad_size(Dch) || bad_size(L) || bad_size(N)) return SS_ERR_SHAPE;
   if (Bsz > 65535 || product_too_big(Bsz, Dch, L)) return SS_ERR_SHAPE;
-  if (N != 16) return SS_ERR_N_UNSUPPORTED;
+  if (!fwd_n_ok(N)) return SS_ERR_N_UNSUPPORTED;
   const bool work = Bsz > 0 && Dch > 0 && L > 0;
   if (work && (!u || !delta || !A || !B || !C || !y)) return SS_ERR_NULL;
   if (misaligned(u) || misaligned(delta) || misaligned(A) || misaligned(B) || misaligned(C) ||
@@ -79,7 +83,7 @@ ss_status run_fwd(const void* u, const void* delta, const float* A, const void* 
     return SS_OK;
   }
   selscan::ScanArgs a{u, delta, A, B, C, D, z, delta_bias, softplus ? 1 : 0,
-                      Bsz, Dch, L, to_dt(dtype), h0};
+                      Bsz, Dch, L, to_dt(dtype), h0, (int)N};
   return cuda_status(selscan::launch_scan_fwd(a, y, h_last, s));
 }
 
@@ -215,7 +219,7 @@ ss_status ss_step(float* h, const void* u_t, const void* delta_t, const float* A
   if (!known_dtype(dtype)) return SS_ERR_DTYPE;
   if (bad_size(Bsz) || bad_size(Dch) || bad_size(N)) return SS_ERR_SHAPE;
   if (Bsz > 65535 || product_too_big(Bsz, Dch, 4)) return SS_ERR_SHAPE;
-  if (N != 16) return SS_ERR_N_UNSUPPORTED;
+  if (!fwd_n_ok(N)) return SS_ERR_N_UNSUPPORTED;
   if (Bsz == 0 || Dch == 0) return SS_OK;
   if (!h || !u_t || !delta_t || !A || !B_t || !C_t || !y_t) return SS_ERR_NULL;
   if (misaligned(h) || misaligned(u_t) || misaligned(delta_t) || misaligned(A) ||
@@ -223,7 +227,7 @@ ss_status ss_step(float* h, const void* u_t, const void* delta_t, const float* A
       misaligned(delta_bias) || misaligned(y_t))
     return SS_ERR_ALIGN;
   selscan::StepArgs a{h, u_t, delta_t, A, B_t, C_t, D, z_t, delta_bias, softplus ? 1 : 0,
-                      Bsz, Dch, to_dt(dtype), y_t};
+                      Bsz, Dch, to_dt(dtype), y_t, (int)N};
   return cuda_status(selscan::launch_step(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

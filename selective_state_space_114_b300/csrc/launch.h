@@ -22,6 +22,7 @@ struct ScanArgs {
   int64_t Bsz, Dch, L;
   Dt dt;
   const float* h0 = nullptr;  // forward only: state before step 0, [Bsz][Dch][N] (nullable = 0)
+  int N = 16;                 // state size: 16; the forward also takes 8, 32, 64
 };
 
 struct BwdOut {
@@ -50,6 +51,7 @@ struct StepArgs {
   int64_t Bsz, Dch;
   Dt dt;
   void* y;
+  int N = 16;  // state size: 8, 16, 32 or 64
 };
 
 // Forward: writes y and (if non-null) h_last.  Requires Bsz*Dch*L > 0.

@@ -284,83 +284,104 @@ __global__ void __launch_bounds__(W * 32)
 }
 
 // ---------------------------------------------------------------------------
-// Row-sequential kernel (rows whose length is a multiple of the 16-byte
-// vector, and enough rows to occupy every SM).
+// Row-sequential kernel (every state size; with 16 states, rows whose length
+// is a multiple of the 16-byte vector and enough rows to occupy every SM).
 //
 // The recurrence of a row is walked in time order by a quad of lanes, each
-// lane holding four of the sixteen states in registers for the whole
-// sequence, so every h_t is formed exactly once (the chunked kernels form it
-// twice: a fold of the chunk and a replay from the carried prefix).  A CTA
-// takes R rows of one batch through the sequence in tiles of T steps, three
-// phases per tile:
+// lane holding NS / 4 of the NS states in registers for the whole sequence,
+// so every h_t is formed exactly once (the chunked kernels form it twice: a
+// fold of the chunk and a replay from the carried prefix).  A CTA takes R
+// rows of one batch through the sequence in tiles of T steps, three phases
+// per tile:
 //   A  element-parallel: delta -> dt = softplus(delta + bias) and dt*u into
 //      shared memory; B and C of the tile converted once to float [t][n]
 //      (all R rows share them);
 //   B  row quads: T steps of the recurrence; per step each lane adds the
-//      C.h terms of its four states and writes that partial to shared
-//      memory (four steps per 128-bit store);
+//      C.h terms of its states and writes that partial to shared memory
+//      (four steps per 128-bit store);
 //   C  element-parallel: y = sum of the four partials + D u, times silu(z),
 //      stored as 16-byte vectors.
 // Phase C of a tile shares the barrier interval of the next tile's phase A.
-// B/C tiles arrive by cp.async one tile ahead; u and delta of the next tile
-// and z of the current one are loaded into registers during phase B.
+// kVec (rows of 16-byte multiples): B/C tiles arrive by cp.async one tile
+// ahead, and u and delta of the next tile and z of the current one are
+// loaded into registers during phase B.  Otherwise every load is an
+// element-wise load checked against L, issued in the phase that uses it.
 // Steps at or past L and rows past Dch get dt = 0 (the state stays put).
 // ---------------------------------------------------------------------------
-template <typename Io, int R, int T, int NR>
+template <typename Io, int R, int T, int NR, int NS>
 struct FwdRowsCfg {
   using E = typename Io::T;
   static constexpr int NT = 4 * R / NR;          // threads: a quad per NR rows
+  static constexpr int SPL = NS / 4;             // states per lane
   static constexpr int V = Io::kVec;             // elements per 16-byte vector
   static constexpr int VPR = T / V;              // vectors of a row in a tile
   static constexpr int NV = R * VPR / NT;        // vectors per thread, phases A/C
   static constexpr int RAWB = T * (int)sizeof(E) + 16;  // raw B/C row bytes (padded)
-  static constexpr int CF_OFF = 16 * T + 16;     // C tile offset from B tile (floats)
+  static constexpr int CF_OFF = NS * T + 16;     // C tile offset from B tile (floats)
   static constexpr int DDS = 2 * T + 4;          // (dt, dt*u) row stride (floats)
   static constexpr int YPS = 4 * T + 16;         // partial row stride (floats)
-  static constexpr size_t raw_bytes = 2ull * 2 * kN * RAWB;
+  static constexpr size_t raw_bytes = 2ull * 2 * NS * RAWB;
   static constexpr size_t smem =
-      raw_bytes + sizeof(float) * ((size_t)CF_OFF + 16 * T + (size_t)R * DDS + (size_t)R * YPS);
+      raw_bytes + sizeof(float) * ((size_t)CF_OFF + NS * T + (size_t)R * DDS + (size_t)R * YPS);
   static_assert(NV >= 1 && R * VPR == NV * NT, "whole vectors per thread");
   static_assert(T % 4 == 0 && (RAWB % 16) == 0 && R % (8 * NR) == 0, "tile shape");
+  static_assert(NS % 8 == 0 && NS <= 64, "state pairs per lane");
 };
 
-template <typename Io, int R, int T, int NR>
+// SPL consecutive floats of shared memory (16-byte aligned when SPL % 4 == 0,
+// else 8-byte aligned) as SPL / 2 float2.
+template <int SPL>
+__device__ __forceinline__ void lds_states(const float* p, float2 (&v)[SPL / 2]) {
+  if constexpr (SPL % 4 == 0) {
+#pragma unroll
+    for (int c = 0; c < SPL / 4; ++c) {
+      const float4 w = reinterpret_cast<const float4*>(p)[c];
+      v[2 * c] = make_float2(w.x, w.y);
+      v[2 * c + 1] = make_float2(w.z, w.w);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < SPL / 2; ++c) v[c] = reinterpret_cast<const float2*>(p)[c];
+  }
+}
+
+template <typename Io, int R, int T, int NR, int NS, bool kVec>
 __global__ void __launch_bounds__(4 * R / NR)
     scan_fwd_rows_kernel(ScanArgs p, typename Io::T* __restrict__ y_out, float* __restrict__ h_last) {
   using E = typename Io::T;
-  using Cfg = FwdRowsCfg<Io, R, T, NR>;
-  constexpr int NT = Cfg::NT, V = Cfg::V, VPR = Cfg::VPR, NV = Cfg::NV;
+  using Cfg = FwdRowsCfg<Io, R, T, NR, NS>;
+  constexpr int NT = Cfg::NT, V = Cfg::V, VPR = Cfg::VPR, NV = Cfg::NV, SPL = Cfg::SPL;
   constexpr int RAWE = Cfg::RAWB / (int)sizeof(E);  // raw row stride in elements
   extern __shared__ float4 smem4[];
   char* base = reinterpret_cast<char*>(smem4);
-  E* raw = reinterpret_cast<E*>(base);  // [2 buffers][2 * kN rows][RAWE]
+  E* raw = reinterpret_cast<E*>(base);  // [2 buffers][2 * NS rows][RAWE]
   float* Bf = reinterpret_cast<float*>(base + Cfg::raw_bytes);
   float* Cf = Bf + Cfg::CF_OFF;
-  float* dd = Cf + 16 * T;  // [R][DDS]
+  float* dd = Cf + NS * T;  // [R][DDS]
   float* yp = dd + R * Cfg::DDS;  // [R][YPS]
 
   const int tid = threadIdx.x;
   const int64_t b = blockIdx.y, L = p.L, Dch = p.Dch;
   const int64_t d0 = (int64_t)blockIdx.x * R;
-  const E* Bb = static_cast<const E*>(p.B) + b * kN * L;
-  const E* Cb = static_cast<const E*>(p.C) + b * kN * L;
+  const E* Bb = static_cast<const E*>(p.B) + b * NS * L;
+  const E* Cb = static_cast<const E*>(p.C) + b * NS * L;
 
-  // recurrence lane: rows qr + j R / NR (j < NR), states 4 qk .. 4 qk + 3
+  // recurrence lane: rows qr + j R / NR (j < NR), states SPL qk .. SPL qk + SPL - 1
   const int qr = tid >> 2, qk = tid & 3;
-  float2 A01[NR], A23[NR], h01[NR], h23[NR];
+  float2 A2[NR][SPL / 2], h[NR][SPL / 2];
 #pragma unroll
   for (int j = 0; j < NR; ++j) {
     const int64_t qd = d0 + qr + j * (R / NR);
-    A01[j] = A23[j] = h01[j] = h23[j] = make_float2(0.f, 0.f);
-    if (qd < Dch) {
-      const float4 a = *reinterpret_cast<const float4*>(p.A + qd * kN + 4 * qk);
-      A01[j] = make_float2(a.x * kLog2e, a.y * kLog2e);
-      A23[j] = make_float2(a.z * kLog2e, a.w * kLog2e);
-      if (p.h0) {
-        const float4 h = *reinterpret_cast<const float4*>(p.h0 + ((b * Dch + qd) * kN + 4 * qk));
-        h01[j] = make_float2(h.x, h.y);
-        h23[j] = make_float2(h.z, h.w);
-      }
+    const bool ok = qd < Dch;
+    const int64_t hrow = b * Dch + (ok ? qd : 0);
+#pragma unroll
+    for (int c = 0; c < SPL / 2; ++c) {
+      const int n = SPL * qk + 2 * c;
+      const float2 a = ok ? *reinterpret_cast<const float2*>(p.A + qd * NS + n)
+                          : make_float2(0.f, 0.f);
+      A2[j][c] = make_float2(a.x * kLog2e, a.y * kLog2e);
+      h[j][c] = (ok && p.h0) ? *reinterpret_cast<const float2*>(p.h0 + hrow * NS + n)
+                             : make_float2(0.f, 0.f);
     }
   }
 
@@ -382,17 +403,19 @@ __global__ void __launch_bounds__(4 * R / NR)
     const int64_t row = b * Dch + (ev[m] ? d : 0);
     ebias[m] = (ev[m] && p.delta_bias) ? p.delta_bias[d] : 0.f;
     eD[m] = (ev[m] && p.D) ? p.D[d] : 0.f;
-    eu[m] = static_cast<const E*>(p.u) + row * L + es[m] * V;
-    edl[m] = static_cast<const E*>(p.delta) + row * L + es[m] * V;
-    ez[m] = p.z ? static_cast<const E*>(p.z) + row * L + es[m] * V : nullptr;
-    ey[m] = y_out + row * L + es[m] * V;
+    // row bases (element-wise path) or the lane's first vector (kVec)
+    const int64_t off = row * L + (kVec ? es[m] * V : 0);
+    eu[m] = static_cast<const E*>(p.u) + off;
+    edl[m] = static_cast<const E*>(p.delta) + off;
+    ez[m] = p.z ? static_cast<const E*>(p.z) + off : nullptr;
+    ey[m] = y_out + off;
   }
   const uint4 zero4 = make_uint4(0, 0, 0, 0);
 
   auto issue_bc = [&](int64_t t0, E* dst) {
-    for (int i = tid; i < 2 * kN * VPR; i += NT) {
-      const int rr = i / VPR, s = i % VPR;  // rr = w * kN + n
-      const E* src = (rr < kN ? Bb + (int64_t)rr * L : Cb + (int64_t)(rr - kN) * L);
+    for (int i = tid; i < 2 * NS * VPR; i += NT) {
+      const int rr = i / VPR, s = i % VPR;  // rr = w * NS + n
+      const E* src = (rr < NS ? Bb + (int64_t)rr * L : Cb + (int64_t)(rr - NS) * L);
       const int64_t t = t0 + s * V;
       const bool in = t < L;
       cp_async16(dst + rr * RAWE + s * V, in ? (const void*)(src + t) : (const void*)src,
@@ -400,20 +423,22 @@ __global__ void __launch_bounds__(4 * R / NR)
     }
   };
 
-  issue_bc(0, raw);
-  cp_async_commit();
   uint4 ru[NV], rd[NV], rz[NV], ru_cur[NV];
+  if constexpr (kVec) {
+    issue_bc(0, raw);
+    cp_async_commit();
 #pragma unroll
-  for (int m = 0; m < NV; ++m) {
-    const bool in = ev[m] && es[m] * V < L;
-    ru[m] = in ? ldg_nc_v4(eu[m]) : zero4;
-    rd[m] = in ? ldg_nc_v4(edl[m]) : zero4;
-    rz[m] = zero4;
-    ru_cur[m] = zero4;
+    for (int m = 0; m < NV; ++m) {
+      const bool in = ev[m] && es[m] * V < L;
+      ru[m] = in ? ldg_nc_v4(eu[m]) : zero4;
+      rd[m] = in ? ldg_nc_v4(edl[m]) : zero4;
+      rz[m] = zero4;
+      ru_cur[m] = zero4;
+    }
   }
 
   for (int64_t t0 = 0, i = 0;; t0 += T, ++i) {
-    cp_async_wait_all();
+    if constexpr (kVec) cp_async_wait_all();
     __syncthreads();  // tile i's B/C landed; phase B of tile i-1 done
 
     // ---- phase C of tile i-1
@@ -425,10 +450,10 @@ __global__ void __launch_bounds__(4 * R / NR)
         if (!ev[m] || t >= L) continue;
         const int rot = (V == 8 ? es[m] : es[m] >> 1) & 3;  // bank-conflict-free order
         const float4* prow = reinterpret_cast<const float4*>(yp + er[m] * Cfg::YPS);
-        float y[V], u[V];
+        float y[V], u[V], zz[V];
 #pragma unroll
-        for (int h = 0; h < V / 4; ++h) {
-          const int g = es[m] * (V / 4) + h;
+        for (int hh = 0; hh < V / 4; ++hh) {
+          const int g = es[m] * (V / 4) + hh;
           float2 lo = make_float2(0.f, 0.f), hi = lo;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
@@ -436,52 +461,72 @@ __global__ void __launch_bounds__(4 * R / NR)
             lo = add2(lo, make_float2(q.x, q.y));
             hi = add2(hi, make_float2(q.z, q.w));
           }
-          y[4 * h] = lo.x;
-          y[4 * h + 1] = lo.y;
-          y[4 * h + 2] = hi.x;
-          y[4 * h + 3] = hi.y;
+          y[4 * hh] = lo.x;
+          y[4 * hh + 1] = lo.y;
+          y[4 * hh + 2] = hi.x;
+          y[4 * hh + 3] = hi.y;
         }
-        Io::unpack(ru_cur[m], u);
+        if constexpr (kVec) {
+          Io::unpack(ru_cur[m], u);
+          if (ez[m]) Io::unpack(rz[m], zz);
+        } else {
+          load_kt<Io, V, false>(eu[m], t, L, true, u);
+          load_kt<Io, V, false>(ez[m], t, L, ez[m] != nullptr, zz);
+        }
 #pragma unroll
         for (int e = 0; e < V; ++e) y[e] = fmaf(eD[m], u[e], y[e]);
         if (ez[m]) {
-          float zz[V];
-          Io::unpack(rz[m], zz);
 #pragma unroll
           for (int e = 0; e < V; ++e) y[e] *= zz[e] * sigmoid_f(zz[e]);
         }
-        stg_v4(ey[m] + tp, Io::pack(y));
+        if constexpr (kVec)
+          stg_v4(ey[m] + tp, Io::pack(y));
+        else
+          store_kt<Io, V, false>(ey[m], t, L, true, y);
       }
     }
     if (t0 >= L) break;
 
     // ---- phase A of tile i
-    {
-      const E* rb = raw + (i & 1) * (2 * kN * RAWE);
-      for (int it = tid; it < 2 * kN * VPR; it += NT) {
-        const int w = (it >> 4) & 1, n = it & 15, ts = it >> 5;
+    if constexpr (kVec) {
+      const E* rb = raw + (i & 1) * (2 * NS * RAWE);
+      for (int it = tid; it < 2 * NS * VPR; it += NT) {
+        const int rr = it % (2 * NS), ts = it / (2 * NS);  // rr = w * NS + n
         float f[V];
-        Io::unpack(*reinterpret_cast<const uint4*>(rb + (w * kN + n) * RAWE + ts * V), f);
-        float* X = w ? Cf : Bf;
+        Io::unpack(*reinterpret_cast<const uint4*>(rb + rr * RAWE + ts * V), f);
+        float* X = rr < NS ? Bf + rr : Cf + (rr - NS);
 #pragma unroll
-        for (int e = 0; e < V; ++e) X[(ts * V + e) * kN + n] = f[e];
+        for (int e = 0; e < V; ++e) X[(ts * V + e) * NS] = f[e];
+      }
+      if (t0 + T < L) issue_bc(t0 + T, raw + ((i + 1) & 1) * (2 * NS * RAWE));
+      cp_async_commit();
+    } else {
+      for (int it = tid; it < 2 * NS * T; it += NT) {
+        const int rr = it / T, tt = it % T;  // consecutive threads: consecutive steps
+        const int64_t t = t0 + tt;
+        const E* src = rr < NS ? Bb + (int64_t)rr * L : Cb + (int64_t)(rr - NS) * L;
+        float* X = rr < NS ? Bf + rr : Cf + (rr - NS);
+        X[tt * NS] = t < L ? Io::to_f(src[t]) : 0.f;
       }
     }
-    if (t0 + T < L) issue_bc(t0 + T, raw + ((i + 1) & 1) * (2 * kN * RAWE));
-    cp_async_commit();
 #pragma unroll
     for (int m = 0; m < NV; ++m) {
       const int64_t t = t0 + es[m] * V;
       const bool in = ev[m] && t < L;
       float u[V], dl[V];
-      Io::unpack(ru[m], u);
-      Io::unpack(rd[m], dl);
+      if constexpr (kVec) {
+        Io::unpack(ru[m], u);
+        Io::unpack(rd[m], dl);
+      } else {
+        load_kt<Io, V, false>(eu[m], t, L, ev[m], u);
+        load_kt<Io, V, false>(edl[m], t, L, ev[m], dl);
+      }
       float q[2 * V];
 #pragma unroll
       for (int e = 0; e < V; ++e) {
         const float x = dl[e] + ebias[m];
         float dt = p.softplus ? softplus_fast(x) : x;
-        dt = in ? dt : 0.f;
+        dt = (in && (kVec || t + e < L)) ? dt : 0.f;
         q[2 * e] = dt;
         q[2 * e + 1] = dt * u[e];
       }
@@ -489,19 +534,21 @@ __global__ void __launch_bounds__(4 * R / NR)
 #pragma unroll
       for (int c = 0; c < V / 2; ++c)
         dst[c] = make_float4(q[4 * c], q[4 * c + 1], q[4 * c + 2], q[4 * c + 3]);
-      // registers for phase C of this tile and phase A of the next one
-      ru_cur[m] = ru[m];
-      rz[m] = (in && ez[m]) ? ldg_nc_v4(ez[m] + t0) : zero4;
-      const bool nin = ev[m] && t + T < L;
-      ru[m] = nin ? ldg_nc_v4(eu[m] + t0 + T) : zero4;
-      rd[m] = nin ? ldg_nc_v4(edl[m] + t0 + T) : zero4;
+      if constexpr (kVec) {
+        // registers for phase C of this tile and phase A of the next one
+        ru_cur[m] = ru[m];
+        rz[m] = (in && ez[m]) ? ldg_nc_v4(ez[m] + t0) : zero4;
+        const bool nin = ev[m] && t + T < L;
+        ru[m] = nin ? ldg_nc_v4(eu[m] + t0 + T) : zero4;
+        rd[m] = nin ? ldg_nc_v4(edl[m] + t0 + T) : zero4;
+      }
     }
     __syncthreads();  // (dt, dt*u) and the B/C tile ready; phase C of tile i-1 done
 
     // ---- phase B of tile i
     {
-      const float4* B4 = reinterpret_cast<const float4*>(Bf) + qk;
-      const float4* C4 = reinterpret_cast<const float4*>(Cf) + qk;
+      const float* Bq = Bf + SPL * qk;
+      const float* Cq = Cf + SPL * qk;
 #pragma unroll 2
       for (int g = 0; g < T / 4; ++g) {
         float dts[NR][4], dus[NR][4], yv[NR][4];
@@ -515,18 +562,21 @@ __global__ void __launch_bounds__(4 * R / NR)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int t = 4 * g + e;
-          const float4 bv = B4[4 * t], cv = C4[4 * t];
+          float2 bv[SPL / 2], cv[SPL / 2];
+          lds_states<SPL>(Bq + t * NS, bv);
+          lds_states<SPL>(Cq + t * NS, cv);
 #pragma unroll
           for (int j = 0; j < NR; ++j) {
             const float2 dt2 = make_float2(dts[j][e], dts[j][e]);
-            const float2 e01 = mul2(dt2, A01[j]), e23 = mul2(dt2, A23[j]);
-            const float2 a01 = make_float2(ex2f(e01.x), ex2f(e01.y));
-            const float2 a23 = make_float2(ex2f(e23.x), ex2f(e23.y));
             const float2 du2 = make_float2(dus[j][e], dus[j][e]);
-            h01[j] = fma2(a01, h01[j], mul2(du2, make_float2(bv.x, bv.y)));
-            h23[j] = fma2(a23, h23[j], mul2(du2, make_float2(bv.z, bv.w)));
-            const float2 yy =
-                fma2(make_float2(cv.z, cv.w), h23[j], mul2(make_float2(cv.x, cv.y), h01[j]));
+            float2 yy = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < SPL / 2; ++c) {
+              const float2 ee = mul2(dt2, A2[j][c]);
+              const float2 a = make_float2(ex2f(ee.x), ex2f(ee.y));
+              h[j][c] = fma2(a, h[j][c], mul2(du2, bv[c]));
+              yy = c ? fma2(cv[c], h[j][c], yy) : mul2(cv[c], h[j][c]);
+            }
             yv[j][e] = yy.x + yy.y;
           }
         }
@@ -541,17 +591,19 @@ __global__ void __launch_bounds__(4 * R / NR)
 #pragma unroll
     for (int j = 0; j < NR; ++j) {
       const int64_t qd = d0 + qr + j * (R / NR);
-      if (qd < Dch)
-        *reinterpret_cast<float4*>(h_last + (b * Dch + qd) * kN + 4 * qk) =
-            make_float4(h01[j].x, h01[j].y, h23[j].x, h23[j].y);
+      if (qd < Dch) {
+#pragma unroll
+        for (int c = 0; c < SPL / 2; ++c)
+          *reinterpret_cast<float2*>(h_last + (b * Dch + qd) * NS + SPL * qk + 2 * c) = h[j][c];
+      }
     }
   }
 }
 
-template <typename Io, int R, int T, int NR>
+template <typename Io, int R, int T, int NR, int NS, bool kVec>
 static cudaError_t launch_fwd_rows(const ScanArgs& a, void* y, float* h_last, cudaStream_t s) {
-  using Cfg = FwdRowsCfg<Io, R, T, NR>;
-  auto kern = scan_fwd_rows_kernel<Io, R, T, NR>;
+  using Cfg = FwdRowsCfg<Io, R, T, NR, NS>;
+  auto kern = scan_fwd_rows_kernel<Io, R, T, NR, NS, kVec>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::smem);
   if (e != cudaSuccess) return e;
@@ -591,24 +643,48 @@ static cudaError_t launch_fwd_t(const ScanArgs& a, void* y, float* h_last, cudaS
 // (bf16 / fp16: 4 warps, 16 steps per lane; fp32: 8 warps, 8 steps per
 // lane), which splits the sequence across lanes.  Other lengths take the
 // element-wise kernel.
+// State sizes other than 16 always take the row-sequential kernel (32
+// channels per CTA, one row per quad), with element-wise loads when the rows
+// are not 16-byte multiples.
 constexpr int64_t kRowsKernelMinRows = 8192;
 
+template <typename Io, int NS>
+static cudaError_t launch_fwd_ns(const ScanArgs& a, void* y, float* h_last, cudaStream_t s) {
+  if (a.L % Io::kVec == 0) return launch_fwd_rows<Io, 32, 32, 1, NS, true>(a, y, h_last, s);
+  return launch_fwd_rows<Io, 32, 32, 1, NS, false>(a, y, h_last, s);
+}
+
+template <typename Io>
+static cudaError_t launch_fwd_other_n(const ScanArgs& a, void* y, float* h_last, cudaStream_t s) {
+  switch (a.N) {
+    case 8: return launch_fwd_ns<Io, 8>(a, y, h_last, s);
+    case 32: return launch_fwd_ns<Io, 32>(a, y, h_last, s);
+    case 64: return launch_fwd_ns<Io, 64>(a, y, h_last, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t launch_scan_fwd(const ScanArgs& a, void* y, float* h_last, cudaStream_t s) {
+  if (a.N != kN) {
+    if (a.dt == Dt::BF16) return launch_fwd_other_n<IoBf16>(a, y, h_last, s);
+    if (a.dt == Dt::F16) return launch_fwd_other_n<IoF16>(a, y, h_last, s);
+    return launch_fwd_other_n<IoF32>(a, y, h_last, s);
+  }
   const bool many_rows = a.Bsz * a.Dch >= kRowsKernelMinRows;
   if (a.dt == Dt::BF16) {
     if (a.L % IoBf16::kVec == 0)
-      return many_rows ? launch_fwd_rows<IoBf16, 32, 32, 1>(a, y, h_last, s)
+      return many_rows ? launch_fwd_rows<IoBf16, 32, 32, 1, 16, true>(a, y, h_last, s)
                        : launch_fwd_pair<IoBf16, 4, 16>(a, y, h_last, s);
     return launch_fwd_t<IoBf16, 8, false>(a, y, h_last, s);
   }
   if (a.dt == Dt::F16) {
     if (a.L % IoF16::kVec == 0)
-      return many_rows ? launch_fwd_rows<IoF16, 32, 32, 1>(a, y, h_last, s)
+      return many_rows ? launch_fwd_rows<IoF16, 32, 32, 1, 16, true>(a, y, h_last, s)
                        : launch_fwd_pair<IoF16, 4, 16>(a, y, h_last, s);
     return launch_fwd_t<IoF16, 8, false>(a, y, h_last, s);
   }
   if (a.L % IoF32::kVec == 0)
-    return many_rows ? launch_fwd_rows<IoF32, 32, 32, 2>(a, y, h_last, s)
+    return many_rows ? launch_fwd_rows<IoF32, 32, 32, 2, 16, true>(a, y, h_last, s)
                      : launch_fwd_pair<IoF32, 8, 8>(a, y, h_last, s);
   return launch_fwd_t<IoF32, 8, false>(a, y, h_last, s);
 }

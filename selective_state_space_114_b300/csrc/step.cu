@@ -4,9 +4,9 @@
 //   delta = softplus(delta_t + bias); h <- exp(delta A) h + delta B_t u_t;
 //   y_t = (C_t . h + D u_t) silu(z_t)
 // Bandwidth-bound on the float32 state: four threads per (batch, channel) row,
-// each updating four states with one 16-byte load and store, so a warp moves
-// 512 contiguous bytes of h per access; the C.h sum is finished with two
-// shuffles inside the group of four.
+// each updating N / 4 states (with N = 16 one 16-byte load and store, so a
+// warp moves 512 contiguous bytes of h per access); the C.h sum is finished
+// with two shuffles inside the group of four.
 #include "common.cuh"
 #include "launch.h"
 
@@ -14,96 +14,117 @@ namespace selscan {
 
 namespace {
 
-template <typename Io>
-__device__ __forceinline__ void load4(const typename Io::T* p, float (&v)[4]) {
+// SPL consecutive elements as float (SPL = 2: one 4- or 8-byte load; SPL a
+// multiple of 4: 8- or 16-byte loads).
+template <typename Io, int SPL>
+__device__ __forceinline__ void load_spl(const typename Io::T* p, float (&v)[SPL]) {
   using T = typename Io::T;
   if constexpr (sizeof(T) == 2) {
-    const uint2 w = *reinterpret_cast<const uint2*>(p);  // four 16-bit elements
-    const T* e = reinterpret_cast<const T*>(&w);
+    if constexpr (SPL == 2) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+      const T* e = reinterpret_cast<const T*>(&w);
+      v[0] = Io::to_f(e[0]);
+      v[1] = Io::to_f(e[1]);
+    } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = Io::to_f(e[i]);
+      for (int c = 0; c < SPL / 4; ++c) {
+        const uint2 w = reinterpret_cast<const uint2*>(p)[c];  // four 16-bit elements
+        const T* e = reinterpret_cast<const T*>(&w);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[4 * c + i] = Io::to_f(e[i]);
+      }
+    }
+  } else if constexpr (SPL % 4 == 0) {
+#pragma unroll
+    for (int c = 0; c < SPL / 4; ++c) {
+      const float4 w = reinterpret_cast<const float4*>(p)[c];
+      v[4 * c] = w.x;
+      v[4 * c + 1] = w.y;
+      v[4 * c + 2] = w.z;
+      v[4 * c + 3] = w.w;
+    }
   } else {
-    const float4 w = *reinterpret_cast<const float4*>(p);
+    const float2 w = *reinterpret_cast<const float2*>(p);
     v[0] = w.x;
     v[1] = w.y;
-    v[2] = w.z;
-    v[3] = w.w;
   }
 }
 
-// Grid: x = blocks of kStepRowsPerCta channels, y = batch.  Quad qi of a CTA
-// owns channels d0 + qi + 64 m (m < kStepRowsPerThread): each of its loads and
-// stores of h covers 64 consecutive channels (4 KB) per CTA, every thread
-// keeps kStepRowsPerThread 16-byte state loads in flight, and the batch index
-// comes from the grid (no division).
+// Grid: x = blocks of 64 channels, y = batch.  Quad qi of a CTA owns channel
+// d0 + qi; each load and store of h covers 64 consecutive channels per CTA,
+// and the batch index comes from the grid (no division).
 constexpr int kStepThreads = 256;
-constexpr int kStepRowsPerThread = 1;
-constexpr int kStepRowsPerCta = kStepThreads / 4 * kStepRowsPerThread;
+constexpr int kStepRowsPerCta = kStepThreads / 4;
 
-template <typename Io>
+template <typename Io, int NS>
 __global__ void __launch_bounds__(kStepThreads) step_kernel(StepArgs p) {
   using T = typename Io::T;
-  constexpr int M = kStepRowsPerThread;
-  const int q = threadIdx.x & 3;  // states 4q .. 4q+3
-  const int qi = threadIdx.x >> 2;
+  constexpr int SPL = NS / 4;
+  const int q = threadIdx.x & 3;  // states SPL q .. SPL q + SPL - 1
   const int64_t b = blockIdx.y;
-  const int64_t d0 = (int64_t)blockIdx.x * kStepRowsPerCta + qi;
+  const int64_t d = (int64_t)blockIdx.x * kStepRowsPerCta + (threadIdx.x >> 2);
+  const bool valid = d < p.Dch;
+  const int64_t dd = valid ? d : 0;
+  const int64_t rr = b * p.Dch + dd;
 
-  float Bv[4], Cv[4];
-  load4<Io>(static_cast<const T*>(p.B) + b * kN + 4 * q, Bv);
-  load4<Io>(static_cast<const T*>(p.C) + b * kN + 4 * q, Cv);
-  float4 hv[M], Av[M];
-  float uu[M], xx[M], zz[M];
-  bool valid[M];
+  // every load first (rows past Dch read row 0 of the batch and store nothing)
+  float Bv[SPL], Cv[SPL], hv[SPL], Av[SPL];
+  load_spl<Io, SPL>(static_cast<const T*>(p.B) + b * NS + SPL * q, Bv);
+  load_spl<Io, SPL>(static_cast<const T*>(p.C) + b * NS + SPL * q, Cv);
+  load_spl<IoF32, SPL>(p.h + rr * NS + SPL * q, hv);
+  load_spl<IoF32, SPL>(p.A + dd * NS + SPL * q, Av);
+  const float uu = Io::to_f(static_cast<const T*>(p.u)[rr]);
+  const float x = Io::to_f(static_cast<const T*>(p.delta)[rr]) +
+                  (p.delta_bias ? p.delta_bias[dd] : 0.f);
+  const float zz = p.z ? Io::to_f(static_cast<const T*>(p.z)[rr]) : 0.f;
+
+  const float dt = p.softplus ? softplus_fast(x) : x;
+  const float dtu = dt * uu;
+  float yp = 0.f;
 #pragma unroll
-  for (int m = 0; m < M; ++m) {
-    const int64_t d = d0 + 64 * m;
-    valid[m] = d < p.Dch;
-    const int64_t rr = b * p.Dch + (valid[m] ? d : 0);
-    hv[m] = valid[m] ? *reinterpret_cast<const float4*>(p.h + rr * kN + 4 * q)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-    Av[m] = valid[m] ? *reinterpret_cast<const float4*>(p.A + d * kN + 4 * q)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-    uu[m] = valid[m] ? Io::to_f(static_cast<const T*>(p.u)[rr]) : 0.f;
-    xx[m] = valid[m] ? Io::to_f(static_cast<const T*>(p.delta)[rr]) +
-                           (p.delta_bias ? p.delta_bias[d] : 0.f)
-                     : 0.f;
-    zz[m] = (valid[m] && p.z) ? Io::to_f(static_cast<const T*>(p.z)[rr]) : 0.f;
+  for (int i = 0; i < SPL; ++i) {
+    hv[i] = fmaf(ex2f(dt * Av[i] * kLog2e), hv[i], dtu * Bv[i]);
+    yp = fmaf(Cv[i], hv[i], yp);
   }
+  if (valid) {
+    float* hp = p.h + rr * NS + SPL * q;
+    if constexpr (SPL % 4 == 0) {
 #pragma unroll
-  for (int m = 0; m < M; ++m) {
-    const int64_t d = d0 + 64 * m;
-    const int64_t rr = b * p.Dch + (valid[m] ? d : 0);
-    const float dt = p.softplus ? softplus_fast(xx[m]) : xx[m];
-    const float dtu = dt * uu[m];
-    float4 h = hv[m];
-    h.x = fmaf(ex2f(dt * Av[m].x * kLog2e), h.x, dtu * Bv[0]);
-    h.y = fmaf(ex2f(dt * Av[m].y * kLog2e), h.y, dtu * Bv[1]);
-    h.z = fmaf(ex2f(dt * Av[m].z * kLog2e), h.z, dtu * Bv[2]);
-    h.w = fmaf(ex2f(dt * Av[m].w * kLog2e), h.w, dtu * Bv[3]);
-    if (valid[m]) *reinterpret_cast<float4*>(p.h + rr * kN + 4 * q) = h;
-    float yp = fmaf(Cv[0], h.x, fmaf(Cv[1], h.y, fmaf(Cv[2], h.z, Cv[3] * h.w)));
-    yp += __shfl_xor_sync(0xffffffffu, yp, 1);
-    yp += __shfl_xor_sync(0xffffffffu, yp, 2);
-    if (valid[m] && q == 0) {
-      float y = fmaf(p.D ? p.D[d] : 0.f, uu[m], yp);
-      if (p.z) y *= zz[m] * sigmoid_f(zz[m]);
-      static_cast<T*>(p.y)[rr] = Io::from_f(y);
+      for (int c = 0; c < SPL / 4; ++c)
+        reinterpret_cast<float4*>(hp)[c] =
+            make_float4(hv[4 * c], hv[4 * c + 1], hv[4 * c + 2], hv[4 * c + 3]);
+    } else {
+      *reinterpret_cast<float2*>(hp) = make_float2(hv[0], hv[1]);
     }
   }
+  yp += __shfl_xor_sync(0xffffffffu, yp, 1);
+  yp += __shfl_xor_sync(0xffffffffu, yp, 2);
+  if (valid && q == 0) {
+    float y = fmaf(p.D ? p.D[d] : 0.f, uu, yp);
+    if (p.z) y *= zz * sigmoid_f(zz);
+    static_cast<T*>(p.y)[rr] = Io::from_f(y);
+  }
+}
+
+template <typename Io>
+cudaError_t launch_step_t(const StepArgs& a, const dim3& grid, cudaStream_t s) {
+  switch (a.N) {
+    case 8: step_kernel<Io, 8><<<grid, kStepThreads, 0, s>>>(a); break;
+    case 16: step_kernel<Io, 16><<<grid, kStepThreads, 0, s>>>(a); break;
+    case 32: step_kernel<Io, 32><<<grid, kStepThreads, 0, s>>>(a); break;
+    case 64: step_kernel<Io, 64><<<grid, kStepThreads, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_step(const StepArgs& a, cudaStream_t s) {
   const dim3 grid((unsigned)((a.Dch + kStepRowsPerCta - 1) / kStepRowsPerCta), (unsigned)a.Bsz);
-  if (a.dt == Dt::BF16)
-    step_kernel<IoBf16><<<grid, kStepThreads, 0, s>>>(a);
-  else if (a.dt == Dt::F16)
-    step_kernel<IoF16><<<grid, kStepThreads, 0, s>>>(a);
-  else
-    step_kernel<IoF32><<<grid, kStepThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  if (a.dt == Dt::BF16) return launch_step_t<IoBf16>(a, grid, s);
+  if (a.dt == Dt::F16) return launch_step_t<IoF16>(a, grid, s);
+  return launch_step_t<IoF32>(a, grid, s);
 }
 
 }  // namespace selscan

@@ -55,8 +55,8 @@ def fwd(**kw):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(dtype=7), DTYPE),
-    (dict(N=8), NUNS),
-    (dict(N=32), NUNS),
+    (dict(N=12), NUNS),
+    (dict(N=128), NUNS),
     (dict(L=-1), SHAPE),
     (dict(Bsz=-3), SHAPE),
     (dict(Bsz=70000), SHAPE),
@@ -105,6 +105,7 @@ def bwd(**kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(dtype=5), DTYPE),
     (dict(N=4), NUNS),
+    (dict(N=32), NUNS),             # the backward takes N = 16 only
     (dict(L=-5), SHAPE),
     (dict(dy=None), NULL),
     (dict(dB=None), NULL),
@@ -131,7 +132,8 @@ def step(**kw):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(dtype=3), DTYPE),
-    (dict(N=64), NUNS),
+    (dict(N=128), NUNS),
+    (dict(N=4), NUNS),
     (dict(Dch=-1), SHAPE),
     (dict(Bsz=65536), SHAPE),
     (dict(h=None), NULL),
@@ -158,7 +160,7 @@ def fwd_from_state(**kw):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(dtype=7), DTYPE), (dict(N=32), NUNS), (dict(L=-1), SHAPE), (dict(u=None), NULL),
+    (dict(dtype=7), DTYPE), (dict(N=24), NUNS), (dict(L=-1), SHAPE), (dict(u=None), NULL),
     (dict(h0=MIS), ALIGN),
 ])
 def test_fwd_from_state_rejects(kw, code):
