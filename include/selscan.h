@@ -42,8 +42,7 @@
  *     a launch error (cudaGetLastError after the launch); faults during
  *     execution surface at the caller's next synchronisation.
  *   - Outputs are overwritten, never accumulated into.
- *   - N (the state size, d_state) is 16 for every entry point; the forward
- *     scans and the step also take 8, 32 and 64 (SS_ERR_N_UNSUPPORTED
+ *   - N (the state size, d_state) is 8, 16, 32 or 64 (SS_ERR_N_UNSUPPORTED
  *     otherwise).  N = 16 is the tuned configuration.
  *   - Bsz is at most 65535 for the scan and step entry points (SS_ERR_SHAPE
  *     otherwise): the batch index is a grid dimension.

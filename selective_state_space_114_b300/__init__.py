@@ -17,8 +17,8 @@ and the autograd wrapper ``selective_scan`` (SelectiveScanFn).
 
 Layouts (channel-major, time innermost): u, delta, z, y: (Bsz, Dch, L);
 B, C: (Bsz, N, L); A: (Dch, N) float32; D, delta_bias: (Dch,) float32;
-h: (Bsz, Dch, N) float32.  N = 16 everywhere; the forward scans and the step
-also take N = 8, 32, 64.  A model holding activations as (B, L, D) (the
+h: (Bsz, Dch, N) float32.  N is 8, 16, 32 or 64 (16 is the tuned size).  A
+model holding activations as (B, L, D) (the
 "mamba.py" page's module boundary) transposes to (B, D, L) before the scan.
 """
 from __future__ import annotations

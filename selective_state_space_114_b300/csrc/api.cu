@@ -29,8 +29,8 @@ bool known_dtype(ss_dtype d) { return d == SS_F32 || d == SS_BF16 || d == SS_F16
 
 Dt to_dt(ss_dtype d) { return d == SS_BF16 ? Dt::BF16 : d == SS_F16 ? Dt::F16 : Dt::F32; }
 
-// State sizes of the forward scans and the step (the backward takes 16 only).
-bool fwd_n_ok(int64_t N) { return N == 8 || N == 16 || N == 32 || N == 64; }
+// State sizes every entry point takes.
+bool n_ok(int64_t N) { return N == 8 || N == 16 || N == 32 || N == 64; }
 
 }  // namespace
 
@@ -43,7 +43,7 @@ const char* ss_status_str(ss_status s) {
     case SS_ERR_SHAPE: return "SS_ERR_SHAPE: a size is negative or too large";
     case SS_ERR_DTYPE: return "SS_ERR_DTYPE: unknown dtype";
     case SS_ERR_N_UNSUPPORTED:
-      return "SS_ERR_N_UNSUPPORTED: N must be 16 (the forward scans and the step also take 8, 32, 64)";
+      return "SS_ERR_N_UNSUPPORTED: N must be 8, 16, 32 or 64";
     case SS_ERR_ALIGN: return "SS_ERR_ALIGN: a pointer is not 16-byte aligned";
     case SS_ERR_WORKSPACE: return "SS_ERR_WORKSPACE: workspace missing, misaligned or too small";
     case SS_ERR_CUDA: return "SS_ERR_CUDA: the CUDA runtime reported an error";
@@ -65,7 +65,7 @@ ss_status run_fwd(const void* u, const void* delta, const float* A, const void* 
   if (!known_dtype(dtype)) return SS_ERR_DTYPE;
   if (bad_size(Bsz) || bad_size(Dch) || bad_size(L) || bad_size(N)) return SS_ERR_SHAPE;
   if (Bsz > 65535 || product_too_big(Bsz, Dch, L)) return SS_ERR_SHAPE;
-  if (!fwd_n_ok(N)) return SS_ERR_N_UNSUPPORTED;
+  if (!n_ok(N)) return SS_ERR_N_UNSUPPORTED;
   const bool work = Bsz > 0 && Dch > 0 && L > 0;
   if (work && (!u || !delta || !A || !B || !C || !y)) return SS_ERR_NULL;
   if (misaligned(u) || misaligned(delta) || misaligned(A) || misaligned(B) || misaligned(C) ||
@@ -112,8 +112,8 @@ ss_status ss_scan_bwd_workspace_size(int64_t Bsz, int64_t Dch, int64_t L, int64_
   if (!known_dtype(dtype)) return SS_ERR_DTYPE;
   if (bad_size(Bsz) || bad_size(Dch) || bad_size(L) || bad_size(N)) return SS_ERR_SHAPE;
   if (Bsz > 65535 || product_too_big(Bsz, Dch, L)) return SS_ERR_SHAPE;
-  if (N != 16) return SS_ERR_N_UNSUPPORTED;
-  *bytes = (Bsz > 0 && Dch > 0 && L > 0) ? selscan::bwd_workspace_bytes(Bsz, Dch, L) : 0;
+  if (!n_ok(N)) return SS_ERR_N_UNSUPPORTED;
+  *bytes = (Bsz > 0 && Dch > 0 && L > 0) ? selscan::bwd_workspace_bytes(Bsz, Dch, L, N) : 0;
   return SS_OK;
 }
 
@@ -131,7 +131,7 @@ ss_status check_bwd(const void* u, const void* delta, const float* A, const void
   if (!known_dtype(dtype)) return SS_ERR_DTYPE;
   if (bad_size(Bsz) || bad_size(Dch) || bad_size(L) || bad_size(N)) return SS_ERR_SHAPE;
   if (Bsz > 65535 || product_too_big(Bsz, Dch, L)) return SS_ERR_SHAPE;
-  if (N != 16) return SS_ERR_N_UNSUPPORTED;
+  if (!n_ok(N)) return SS_ERR_N_UNSUPPORTED;
   *work = Bsz > 0 && Dch > 0 && L > 0;
   if (*work && (!u || !delta || !A || !B || !C || !dy || !du || !ddelta || !dA || !dB || !dC))
     return SS_ERR_NULL;
@@ -144,7 +144,7 @@ ss_status check_bwd(const void* u, const void* delta, const float* A, const void
       misaligned(dC) || misaligned(dD) || misaligned(dz) || misaligned(ddelta_bias))
     return SS_ERR_ALIGN;
   if (*work) {
-    const size_t need = selscan::bwd_workspace_bytes(Bsz, Dch, L);
+    const size_t need = selscan::bwd_workspace_bytes(Bsz, Dch, L, N);
     if (!workspace || misaligned(workspace) || workspace_bytes < need) return SS_ERR_WORKSPACE;
   }
   return SS_OK;
@@ -185,7 +185,7 @@ ss_status run_bwd(int phase, const void* u, const void* delta, const float* A, c
     return SS_OK;
   }
   selscan::ScanArgs a{u, delta, A, B, C, D, z, delta_bias, softplus ? 1 : 0,
-                      Bsz, Dch, L, to_dt(dtype)};
+                      Bsz, Dch, L, to_dt(dtype), nullptr, (int)N};
   selscan::BwdOut o{dy, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias};
   for (int ph = 0; ph < 3; ++ph) {
     if (phase >= 0 && ph != phase) continue;
@@ -219,7 +219,7 @@ ss_status ss_step(float* h, const void* u_t, const void* delta_t, const float* A
   if (!known_dtype(dtype)) return SS_ERR_DTYPE;
   if (bad_size(Bsz) || bad_size(Dch) || bad_size(N)) return SS_ERR_SHAPE;
   if (Bsz > 65535 || product_too_big(Bsz, Dch, 4)) return SS_ERR_SHAPE;
-  if (!fwd_n_ok(N)) return SS_ERR_N_UNSUPPORTED;
+  if (!n_ok(N)) return SS_ERR_N_UNSUPPORTED;
   if (Bsz == 0 || Dch == 0) return SS_OK;
   if (!h || !u_t || !delta_t || !A || !B_t || !C_t || !y_t) return SS_ERR_NULL;
   if (misaligned(h) || misaligned(u_t) || misaligned(delta_t) || misaligned(A) ||

@@ -404,31 +404,31 @@ __device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wai
 // X = B (w = 0) or C (w = 1): lane j of a row reads its KT steps of the
 // state pair q as KT/2 conflict-free 128-bit loads.
 // ---------------------------------------------------------------------------
-template <typename Io, int CH>
+template <typename Io, int CH, int NS = kN>
 __device__ __forceinline__ void issue_raw_bc(const typename Io::T* __restrict__ Bb,
                                              const typename Io::T* __restrict__ Cb, int64_t L,
                                              int64_t t0, typename Io::T* raw, int tid, int nthr) {
   using T = typename Io::T;
   constexpr int V = Io::kVec;  // elements per 16 bytes
   constexpr int per_row = CH / V;
-  constexpr int total = 2 * kN * per_row;
+  constexpr int total = 2 * NS * per_row;
   for (int i = tid; i < total; i += nthr) {
-    const int w = i / (kN * per_row);
-    const int rem = i - w * kN * per_row;
+    const int w = i / (NS * per_row);
+    const int rem = i - w * NS * per_row;
     const int n = rem / per_row;
     const int tl = (rem - n * per_row) * V;
     const int64_t t = t0 + tl;
     const T* row = (w ? Cb : Bb) + (int64_t)n * L;
     const bool in = t < L;  // whole vector in or out: L % V == 0
-    cp_async16(raw + (w * kN + n) * CH + tl, in ? (const void*)(row + t) : (const void*)row,
+    cp_async16(raw + (w * NS + n) * CH + tl, in ? (const void*)(row + t) : (const void*)row,
                in ? 16 : 0);
   }
 }
 
-template <typename Io, int CH, int KT, int RL>
+template <typename Io, int CH, int KT, int RL, int NS = kN>
 __device__ __forceinline__ void raw_to_pairs(const typename Io::T* raw, float4* pairs, int tid,
                                              int nthr) {
-  constexpr int items = 2 * (kN / 2) * (CH / 8);  // (w, q, octet of steps)
+  constexpr int items = 2 * (NS / 2) * (CH / 8);  // (w, q, octet of steps)
   constexpr int m = KT / 8;                         // octets per lane segment
   static_assert(CH / 8 == RL * m, "chunk = RL segments of KT steps");
   for (int i = tid; i < items; i += nthr) {
@@ -436,9 +436,9 @@ __device__ __forceinline__ void raw_to_pairs(const typename Io::T* raw, float4* 
     // 16-byte stores of a quarter-warp fill one contiguous 128-byte line
     const int x = i % (CH / 8);
     const int o = m * (x % RL) + x / RL;
-    const int wq = i / (CH / 8);  // w * 8 + q
-    const int w = wq >> 3, q = wq & 7;
-    const typename Io::T* r0 = raw + (w * kN + 2 * q) * CH + 8 * o;
+    const int wq = i / (CH / 8);  // w * NS / 2 + q
+    const int w = wq / (NS / 2), q = wq % (NS / 2);
+    const typename Io::T* r0 = raw + (w * NS + 2 * q) * CH + 8 * o;
     const typename Io::T* r1 = r0 + CH;
     float v0[8], v1[8];
 #pragma unroll
@@ -456,15 +456,15 @@ __device__ __forceinline__ void raw_to_pairs(const typename Io::T* raw, float4* 
 }
 
 // Scalar (any L) version: read B/C of the chunk straight into the pair layout.
-template <typename Io, int CH, int KT, int RL>
+template <typename Io, int CH, int KT, int RL, int NS = kN>
 __device__ __forceinline__ void load_pairs_scalar(const typename Io::T* __restrict__ Bb,
                                                   const typename Io::T* __restrict__ Cb, int64_t L,
                                                   int64_t t0, float4* pairs, int tid, int nthr) {
-  constexpr int items = 2 * (kN / 2) * (CH / 2);  // (w, q, step pair)
+  constexpr int items = 2 * (NS / 2) * (CH / 2);  // (w, q, step pair)
   for (int i = tid; i < items; i += nthr) {
     const int k2 = i % (CH / 2);
     const int wq = i / (CH / 2);
-    const int w = wq >> 3, q = wq & 7;
+    const int w = wq / (NS / 2), q = wq % (NS / 2);
     const int t = 2 * k2;
     const typename Io::T* r0 = (w ? Cb : Bb) + (int64_t)(2 * q) * L;
     const typename Io::T* r1 = r0 + L;

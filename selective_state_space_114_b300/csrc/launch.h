@@ -22,7 +22,7 @@ struct ScanArgs {
   int64_t Bsz, Dch, L;
   Dt dt;
   const float* h0 = nullptr;  // forward only: state before step 0, [Bsz][Dch][N] (nullable = 0)
-  int N = 16;                 // state size: 16; the forward also takes 8, 32, 64
+  int N = 16;                 // state size: 8, 16, 32 or 64
 };
 
 struct BwdOut {
@@ -60,7 +60,7 @@ cudaError_t launch_scan_fwd(const ScanArgs& a, void* y, float* h_last, cudaStrea
 // Backward workspace size (bytes) and the launch of one of its three stages
 // (phase 0: segment states, 1: reverse pass, 2: reduction of the partials).
 // Requires Bsz*Dch*L > 0.
-size_t bwd_workspace_bytes(int64_t Bsz, int64_t Dch, int64_t L);
+size_t bwd_workspace_bytes(int64_t Bsz, int64_t Dch, int64_t L, int64_t N);
 cudaError_t launch_scan_bwd(int phase, const ScanArgs& a, const BwdOut& o, void* ws,
                             cudaStream_t s);
 

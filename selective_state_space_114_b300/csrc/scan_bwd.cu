@@ -16,8 +16,9 @@
 // The sequence is cut into chunks of kBwdChunk steps that are processed
 // independently once the state entering each chunk (forward) and the adjoint
 // entering it from the later chunk (reverse) are known:
-//  stage 0a  bwd_summary: one thread per (row, chunk) walks the chunk in time
-//            order with all 16 states in registers (no cross-lane traffic) and
+//  stage 0a  bwd_summary: one thread per (row, chunk, group of up to 16
+//            states) walks the chunk in time order with the group's states in
+//            registers (no cross-lane traffic) and
 //            records the chunk's affine summaries: S = state at the chunk end
 //            from a zero start, Q = sum_t (prod_{k<=t} a_k) yhat_t C_t (the
 //            adjoint carry it sends back from a zero incoming carry), and
@@ -54,17 +55,17 @@ struct WsLayout {
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-inline WsLayout ws_layout(int64_t Bsz, int64_t Dch, int64_t L) {
+inline WsLayout ws_layout(int64_t Bsz, int64_t Dch, int64_t L, int64_t N) {
   WsLayout w;
   w.nchunks = (L + kBwdChunk - 1) / kBwdChunk;
   w.blocks = (Dch + kRowBlock - 1) / kRowBlock;
   const size_t rc = (size_t)(Bsz * Dch) * w.nchunks;  // (row, chunk) pairs
   size_t off = 0;
-  w.sumS = off;  off = align256(off + sizeof(float) * rc * kN);
-  w.sumQ = off;  off = align256(off + sizeof(float) * rc * kN);
+  w.sumS = off;  off = align256(off + sizeof(float) * rc * N);
+  w.sumQ = off;  off = align256(off + sizeof(float) * rc * N);
   w.dsum = off;  off = align256(off + sizeof(float) * rc);
-  w.pbc = off;   off = align256(off + sizeof(float) * (size_t)(Bsz * w.blocks) * 2 * kN * L);
-  w.pa = off;    off = align256(off + sizeof(float) * rc * kN);
+  w.pbc = off;   off = align256(off + sizeof(float) * (size_t)(Bsz * w.blocks) * 2 * N * L);
+  w.pa = off;    off = align256(off + sizeof(float) * rc * N);
   w.pd = off;    off = align256(off + sizeof(float) * rc);
   w.pbias = off; off = align256(off + sizeof(float) * rc);
   w.total = off;
@@ -80,17 +81,21 @@ __device__ __forceinline__ float step_delta(float raw, float bias, int softplus)
 // ---------------------------------------------------------------------------
 // 0a. chunk summaries
 // ---------------------------------------------------------------------------
-template <typename Io, bool kVec>
+// NS states in groups of SG = min(NS, 16): grid z = NS / SG, each thread
+// holds the SG states of its group (states SG z .. SG z + SG - 1).
+template <typename Io, bool kVec, int NS>
 __global__ void __launch_bounds__(kSumThreads)
     bwd_summary_kernel(ScanArgs p, BwdOut o, int64_t nrb, float* __restrict__ sumS,
                        float* __restrict__ sumQ, float* __restrict__ dsum_out) {
   using T = typename Io::T;
   constexpr int CH = kBwdChunk;
+  constexpr int SG = NS < 16 ? NS : 16;
   extern __shared__ float4 smem4[];
-  float* sB = reinterpret_cast<float*>(smem4);  // [t][n]
-  float* sC = sB + CH * kN;                      // [t][n]
-  uint4* ring = reinterpret_cast<uint4*>(sC + CH * kN);  // input ring (16-byte rows only)
+  float* sB = reinterpret_cast<float*>(smem4);  // [t][n of the group]
+  float* sC = sB + CH * SG;                      // [t][n of the group]
+  uint4* ring = reinterpret_cast<uint4*>(sC + CH * SG);  // input ring (16-byte rows only)
   const int tid = threadIdx.x;
+  const int n0 = SG * blockIdx.z;
   const int64_t c = blockIdx.x / nrb;
   const int64_t rb = blockIdx.x - c * nrb;
   const int64_t b = blockIdx.y;
@@ -101,36 +106,36 @@ __global__ void __launch_bounds__(kSumThreads)
   const int64_t row = b * p.Dch + (valid ? d : 0);
 
   // stage B, C of (b, chunk) transposed to [t][n]
-  const T* Bb = static_cast<const T*>(p.B) + b * kN * L;
-  const T* Cb = static_cast<const T*>(p.C) + b * kN * L;
-  for (int i = tid; i < 2 * kN * (CH / 8); i += kSumThreads) {
+  const T* Bb = static_cast<const T*>(p.B) + (b * NS + n0) * L;
+  const T* Cb = static_cast<const T*>(p.C) + (b * NS + n0) * L;
+  for (int i = tid; i < 2 * SG * (CH / 8); i += kSumThreads) {
     // consecutive threads -> consecutive states n: the transposed [t][n]
     // stores of a warp land in two 64-byte runs
-    const int n = i % kN;
-    const int wo = i / kN;
+    const int n = i % SG;
+    const int wo = i / SG;
     const int o = wo % (CH / 8), w = wo / (CH / 8);
     const T* src = (w ? Cb : Bb) + (int64_t)n * L + t0 + 8 * o;
     float v[8];
     load_kt<Io, 8, kVec>(src, 0, L - t0 - 8 * o, true, v);
-    float* dst = (w ? sC : sB) + 8 * o * kN + n;
+    float* dst = (w ? sC : sB) + 8 * o * SG + n;
 #pragma unroll
-    for (int s = 0; s < 8; ++s) dst[s * kN] = v[s];
+    for (int s = 0; s < 8; ++s) dst[s * SG] = v[s];
   }
   __syncthreads();
   if (!valid) return;
 
-  float A2[kN];
+  float A2[SG];
 #pragma unroll
-  for (int n = 0; n < kN; ++n) A2[n] = p.A[d * kN + n] * kLog2e;
+  for (int n = 0; n < SG; ++n) A2[n] = p.A[d * NS + n0 + n] * kLog2e;
   const float bias = p.delta_bias ? p.delta_bias[d] : 0.f;
   const T* urow = static_cast<const T*>(p.u) + row * L;
   const T* drow = static_cast<const T*>(p.delta) + row * L;
   const T* zrow = p.z ? static_cast<const T*>(p.z) + row * L : nullptr;
   const T* grow = static_cast<const T*>(o.dy) + row * L;
 
-  float2 S[kN / 2], Q[kN / 2], cp[kN / 2];
+  float2 S[SG / 2], Q[SG / 2], cp[SG / 2];
 #pragma unroll
-  for (int q = 0; q < kN / 2; ++q) {
+  for (int q = 0; q < SG / 2; ++q) {
     S[q] = make_float2(0.f, 0.f);
     Q[q] = make_float2(0.f, 0.f);
     cp[q] = make_float2(1.f, 1.f);
@@ -195,10 +200,10 @@ __global__ void __launch_bounds__(kSumThreads)
       const float dtu = dt * uu[s];
       const float yh = zrow ? gg[s] * zz[s] * sigmoid_f(zz[s]) : gg[s];
       dsum += dt;
-      const float4* bq = reinterpret_cast<const float4*>(sB + (tb + s) * kN);
-      const float4* cq = reinterpret_cast<const float4*>(sC + (tb + s) * kN);
+      const float4* bq = reinterpret_cast<const float4*>(sB + (tb + s) * SG);
+      const float4* cq = reinterpret_cast<const float4*>(sC + (tb + s) * SG);
 #pragma unroll
-      for (int k = 0; k < kN / 4; ++k) {
+      for (int k = 0; k < SG / 4; ++k) {
         const float4 bv = bq[k], cv = cq[k];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -215,43 +220,44 @@ __global__ void __launch_bounds__(kSumThreads)
     }
   }
   const size_t rc = (size_t)row * nch + c;
-  float4* so = reinterpret_cast<float4*>(sumS + rc * kN);
-  float4* qo = reinterpret_cast<float4*>(sumQ + rc * kN);
+  float4* so = reinterpret_cast<float4*>(sumS + rc * NS + n0);
+  float4* qo = reinterpret_cast<float4*>(sumQ + rc * NS + n0);
 #pragma unroll
-  for (int k = 0; k < kN / 4; ++k) {
+  for (int k = 0; k < SG / 4; ++k) {
     so[k] = make_float4(S[2 * k].x, S[2 * k].y, S[2 * k + 1].x, S[2 * k + 1].y);
     qo[k] = make_float4(Q[2 * k].x, Q[2 * k].y, Q[2 * k + 1].x, Q[2 * k + 1].y);
   }
-  dsum_out[rc] = dsum;
+  if (n0 == 0) dsum_out[rc] = dsum;
 }
 
 // ---------------------------------------------------------------------------
 // 0b. chunk carries: sumS[row][c] <- h entering chunk c; sumQ[row][c] <- the
 //     adjoint carry entering chunk c from chunk c+1 (zero for the last).
 // ---------------------------------------------------------------------------
+template <int NS>
 __global__ void bwd_carry_kernel(const float* __restrict__ A, int64_t Bsz, int64_t Dch,
                                  int64_t nch, float* __restrict__ sumS, float* __restrict__ sumQ,
                                  const float* __restrict__ dsum) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= Bsz * Dch * kN) return;
-  const int64_t row = i / kN;
-  const int n = (int)(i % kN);
+  if (i >= Bsz * Dch * NS) return;
+  const int64_t row = i / NS;
+  const int n = (int)(i % NS);
   const int64_t d = row % Dch;
-  const float a2 = A[d * kN + n] * kLog2e;
+  const float a2 = A[d * NS + n] * kLog2e;
   float h = 0.f;
   for (int64_t c = 0; c < nch; ++c) {
     const size_t rc = (size_t)row * nch + c;
     const float P = ex2f(a2 * dsum[rc]);
-    const float s = sumS[rc * kN + n];
-    sumS[rc * kN + n] = h;
+    const float s = sumS[rc * NS + n];
+    sumS[rc * NS + n] = h;
     h = fmaf(P, h, s);
   }
   float rho = 0.f;
   for (int64_t c = nch - 1; c >= 0; --c) {
     const size_t rc = (size_t)row * nch + c;
     const float P = ex2f(a2 * dsum[rc]);
-    const float qv = sumQ[rc * kN + n];
-    sumQ[rc * kN + n] = rho;
+    const float qv = sumQ[rc * NS + n];
+    sumQ[rc * NS + n] = rho;
     rho = fmaf(P, rho, qv);
   }
 }
@@ -268,16 +274,16 @@ __global__ void bwd_carry_kernel(const float* __restrict__ A, int64_t Bsz, int64
 // writes its dB / dC terms to its own slot; after a barrier the 256 threads
 // sum the 16 rows' slots into the block accumulator.
 // ---------------------------------------------------------------------------
-template <int W, typename T, int kSlotBufs>
+template <int W, typename T, int kSlotBufs, int NS>
 struct MainSmem {
   static constexpr int KT = kKTb, RL = kRLb, CH = kBwdChunk, R = 2 * W;
-  static constexpr size_t pairs = sizeof(float4) * 2 * (kN / 2) * (KT / 2) * RL;  // B, C
+  static constexpr size_t pairs = sizeof(float4) * 2 * (NS / 2) * (KT / 2) * RL;  // B, C
   static constexpr size_t slot_row = 2 * CH * 2 + 4;  // [dB,dC][CH][2 states] floats, padded
                                                       // so the two rows of a warp use other banks
   static constexpr size_t slots = sizeof(float) * kSlotBufs * R * slot_row;  // [buffer][row]
-  static constexpr size_t acc = sizeof(float) * 2 * kN * CH;            // [dB,dC][q][CH][2]
-  static constexpr size_t dA = sizeof(float) * R * kN * RL;             // [row][n][j]
-  static constexpr size_t params = sizeof(float) * 4 * R * kN;          // A2, A, h_in, rho_in
+  static constexpr size_t acc = sizeof(float) * 2 * NS * CH;            // [dB,dC][q][CH][2]
+  static constexpr size_t dA = sizeof(float) * R * NS * RL;             // [row][n][j]
+  static constexpr size_t params = sizeof(float) * 4 * R * NS;          // A2, A, h_in, rho_in
   // u, delta, z, dy segments of a pass, [buffer][tensor][vector][thread] 16-byte units
   static constexpr size_t ins = 2ull * 4 * KT * sizeof(T) * (W * 32);
   static constexpr size_t total = pairs + slots + acc + dA + params + ins;
@@ -336,14 +342,14 @@ __device__ __forceinline__ int slot_swizzle(int j) { return 2 * ((j >> 1) & 1); 
 // (pre-gate output, sum lam B, sum A lam a h) in the row's registers, stores
 // the row's dB and dC terms of the pair at dB_lo / dC_lo (state 2q, state 2q+1
 // at +CH) and the lane's dA terms of the two states at dA_lo[0], dA_lo[RL].
-template <int KT, int RL, int CH>
+template <int KT, int RL, int CH, int NS>
 __device__ __forceinline__ void bwd_state_pair(
     int q, int j, int r, bool valid, const float* A2s, const float* Ars, const float* hin_row,
     const float* rin_row, const float4* Bp, const float4* Cp, const float (&dl)[KT],
     const float2 (&du2)[KT], const float2 (&yh2)[KT], float dsum, float2 (&yacc2)[KT],
     float2 (&s12)[KT], float2 (&s22)[KT], float* dB_lo, float* dC_lo, float* dA_lo) {
-    const float2 a2 = *reinterpret_cast<const float2*>(A2s + r * kN + 2 * q);
-    const float2 Ar = *reinterpret_cast<const float2*>(Ars + r * kN + 2 * q);
+    const float2 a2 = *reinterpret_cast<const float2*>(A2s + r * NS + 2 * q);
+    const float2 Ar = *reinterpret_cast<const float2*>(Ars + r * NS + 2 * q);
     const float2 hc = valid ? *reinterpret_cast<const float2*>(hin_row + 2 * q) : make_float2(0.f, 0.f);
     const float2 rcar = valid ? *reinterpret_cast<const float2*>(rin_row + 2 * q) : make_float2(0.f, 0.f);
     const float4* bq = Bp + q * (KT / 2) * RL + j;
@@ -448,13 +454,13 @@ __device__ __forceinline__ void bwd_state_pair(
 
 }
 
-template <typename Io, bool kVec, int W, int kMinBlocks, int kSlotBufs>
+template <typename Io, bool kVec, int W, int kMinBlocks, int kSlotBufs, int NS>
 __global__ void __launch_bounds__(W * 32, kMinBlocks)
     bwd_main_kernel(ScanArgs p, BwdOut o, int64_t nrb, const float* __restrict__ Hin,
                     const float* __restrict__ Rin, float* __restrict__ pBC,
                     float* __restrict__ pA, float* __restrict__ pD, float* __restrict__ pbias) {
   using T = typename Io::T;
-  using Sm = MainSmem<W, T, kSlotBufs>;
+  using Sm = MainSmem<W, T, kSlotBufs, NS>;
   constexpr int KT = kKTb, RL = kRLb, CH = kBwdChunk, R = 2 * W, NT = W * 32;
   constexpr int kPasses = kRowBlock / R;
   constexpr int SR = (int)Sm::slot_row;
@@ -465,13 +471,13 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks)
   float* acc = reinterpret_cast<float*>(sm + Sm::pairs + Sm::slots);
   float* dAs = reinterpret_cast<float*>(sm + Sm::pairs + Sm::slots + Sm::acc);
   float* A2s = reinterpret_cast<float*>(sm + Sm::pairs + Sm::slots + Sm::acc + Sm::dA);
-  float* Ars = A2s + R * kN;
-  float* Hs = Ars + R * kN;   // [row][n] state entering the chunk
-  float* Rs = Hs + R * kN;    // [row][n] adjoint carry entering the chunk
+  float* Ars = A2s + R * NS;
+  float* Hs = Ars + R * NS;   // [row][n] state entering the chunk
+  float* Rs = Hs + R * NS;    // [row][n] adjoint carry entering the chunk
   uint4* ins = reinterpret_cast<uint4*>(sm + Sm::pairs + Sm::slots + Sm::acc + Sm::dA + Sm::params);
   constexpr int kInsBuf = (int)(Sm::ins / 2 / sizeof(uint4));  // uint4 per buffer
   const float4* Bp = pairs;
-  const float4* Cp = pairs + (kN / 2) * (KT / 2) * RL;
+  const float4* Cp = pairs + (NS / 2) * (KT / 2) * RL;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int j = lane >> 1, rs = lane & 1;
@@ -481,14 +487,14 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks)
   const int64_t b = blockIdx.y;
   const int64_t L = p.L, t0 = c * CH;
   const int64_t nch = (L + CH - 1) / CH;
-  const T* Bb = static_cast<const T*>(p.B) + b * kN * L;
-  const T* Cb = static_cast<const T*>(p.C) + b * kN * L;
+  const T* Bb = static_cast<const T*>(p.B) + b * NS * L;
+  const T* Cb = static_cast<const T*>(p.C) + b * NS * L;
 
   if (kVec) {
     // one-shot copy of the chunk's B / C, staged raw in the accumulator area
     T* raw = reinterpret_cast<T*>(acc);
-    static_assert(2 * kN * CH * sizeof(T) <= Sm::acc, "raw staging must fit");
-    issue_raw_bc<Io, CH>(Bb, Cb, L, t0, raw, tid, NT);
+    static_assert(2 * NS * CH * sizeof(T) <= Sm::acc, "raw staging must fit");
+    issue_raw_bc<Io, CH, NS>(Bb, Cb, L, t0, raw, tid, NT);
     cp_async_commit();
     {
       const int64_t d = g * kRowBlock + r;
@@ -498,12 +504,12 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks)
     cp_async_commit();
     cp_async_wait_one();  // B / C landed (the inputs may still be in flight)
     __syncthreads();
-    raw_to_pairs<Io, CH, KT, RL>(raw, pairs, tid, NT);
+    raw_to_pairs<Io, CH, KT, RL, NS>(raw, pairs, tid, NT);
     __syncthreads();
   } else {
-    load_pairs_scalar<Io, CH, KT, RL>(Bb, Cb, L, t0, pairs, tid, NT);
+    load_pairs_scalar<Io, CH, KT, RL, NS>(Bb, Cb, L, t0, pairs, tid, NT);
   }
-  for (int i = tid; i < 2 * kN * CH; i += NT) acc[i] = 0.f;
+  for (int i = tid; i < 2 * NS * CH; i += NT) acc[i] = 0.f;
 
   const int64_t ts = t0 + KT * j;
   float* my_slot0 = slots + (size_t)r * SR + 2 * KT * j;  // + buffer * R * SR
@@ -526,13 +532,13 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks)
     const bool valid = d < p.Dch;
     const int64_t row = b * p.Dch + (valid ? d : 0);
     __syncthreads();  // previous pass done with the per-pass buffers
-    for (int i = tid; i < R * kN; i += NT) {
-      const int64_t dd = d0 + i / kN;
+    for (int i = tid; i < R * NS; i += NT) {
+      const int64_t dd = d0 + i / NS;
       const bool ok = dd < p.Dch;
-      const float av = ok ? p.A[dd * kN + i % kN] : 0.f;
+      const float av = ok ? p.A[dd * NS + i % NS] : 0.f;
       A2s[i] = av * kLog2e;
       Ars[i] = av;
-      const size_t rci = ((size_t)(b * p.Dch + (ok ? dd : 0)) * nch + c) * kN + i % kN;
+      const size_t rci = ((size_t)(b * p.Dch + (ok ? dd : 0)) * nch + c) * NS + i % NS;
       Hs[i] = ok ? Hin[rci] : 0.f;
       Rs[i] = ok ? Rin[rci] : 0.f;
     }
@@ -545,8 +551,8 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks)
     const T* zrow = p.z ? static_cast<const T*>(p.z) + row * L : nullptr;
     const T* grow = static_cast<const T*>(o.dy) + row * L;
     const size_t rc = (size_t)row * nch + c;
-    const float* hin_row = Hs + r * kN;
-    const float* rin_row = Rs + r * kN;
+    const float* hin_row = Hs + r * NS;
+    const float* rin_row = Rs + r * NS;
 
     const uint4* inb = ins + (pass & 1) * kInsBuf;  // this pass's inputs (16-byte rows)
     if (kVec) {
@@ -591,12 +597,12 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks)
     }
 
 #pragma unroll 1
-    for (int q = 0; q < kN / 2; ++q) {
+    for (int q = 0; q < NS / 2; ++q) {
       const int sb = kSlotBufs == 2 ? (q & 1) : 0;
       float* slot = my_slot0 + (size_t)sb * R * SR;
-      bwd_state_pair<KT, RL, CH>(q, j, r, valid, A2s, Ars, hin_row, rin_row, Bp, Cp, dl, du2, yh2,
-                                 dsum, yacc2, s12, s22, slot, slot + 2 * CH,
-                                 dAs + (r * kN + 2 * q) * RL + j);
+      bwd_state_pair<KT, RL, CH, NS>(q, j, r, valid, A2s, Ars, hin_row, rin_row, Bp, Cp, dl, du2,
+                                     yh2, dsum, yacc2, s12, s22, slot, slot + 2 * CH,
+                                     dAs + (r * NS + 2 * q) * RL + j);
 
       // dB / dC of this state pair: sum the rows' slots into the accumulator
       __syncthreads();
@@ -610,7 +616,7 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks)
           lo = add2(lo, make_float2(v.x, v.y));
           hi = add2(hi, make_float2(v.z, v.w));
         }
-        float4* ap = reinterpret_cast<float4*>(acc + ((size_t)sum_wh * (kN / 2) + q) * 2 * CH + sum_st);
+        float4* ap = reinterpret_cast<float4*>(acc + ((size_t)sum_wh * (NS / 2) + q) * 2 * CH + sum_st);
         v = *ap;
         lo = add2(lo, make_float2(v.x, v.y));
         hi = add2(hi, make_float2(v.z, v.w));
@@ -666,41 +672,42 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks)
     }
     // dA of the pass's rows: thread -> (row, state), sum over the 16 segments
     __syncthreads();
-    for (int i = tid; i < R * kN; i += NT) {
-      const int rr = i / kN, n = i % kN;
+    for (int i = tid; i < R * NS; i += NT) {
+      const int rr = i / NS, n = i % NS;
       const int64_t dd = d0 + rr;
-      const float4* src = reinterpret_cast<const float4*>(dAs + (rr * kN + n) * RL);
+      const float4* src = reinterpret_cast<const float4*>(dAs + (rr * NS + n) * RL);
       float sd = 0.f;
 #pragma unroll
       for (int k4 = 0; k4 < RL / 4; ++k4) {
         const float4 v = src[k4];
         sd += (v.x + v.y) + (v.z + v.w);
       }
-      if (dd < p.Dch) pA[((size_t)(b * p.Dch + dd) * nch + c) * kN + n] = sd;
+      if (dd < p.Dch) pA[((size_t)(b * p.Dch + dd) * nch + c) * NS + n] = sd;
     }
   }
   __syncthreads();
   // this block's dB / dC partial for the chunk
-  float* out = pBC + ((size_t)(b * nrb + g) * 2) * kN * L;
-  for (int i = tid; i < 2 * kN * CH; i += NT) {
-    const int whn = i / CH, tt = i % CH;  // (wh * kN + n, t)
-    const int wh = whn / kN, n = whn % kN;
-    if (t0 + tt < L) out[(size_t)whn * L + t0 + tt] = acc[((wh * (kN / 2) + n / 2) * CH + tt) * 2 + (n & 1)];
+  float* out = pBC + ((size_t)(b * nrb + g) * 2) * NS * L;
+  for (int i = tid; i < 2 * NS * CH; i += NT) {
+    const int whn = i / CH, tt = i % CH;  // (wh * NS + n, t)
+    const int wh = whn / NS, n = whn % NS;
+    if (t0 + tt < L) out[(size_t)whn * L + t0 + tt] = acc[((wh * (NS / 2) + n / 2) * CH + tt) * 2 + (n & 1)];
   }
 }
 
 // ---------------------------------------------------------------------------
 // 2. fixed-order reduction of the partials
 // ---------------------------------------------------------------------------
+template <int NS>
 __global__ void bwd_reduce_bc_kernel(const float* __restrict__ pBC, int64_t nrb, int64_t Bsz,
                                      int64_t L, float* __restrict__ dB, float* __restrict__ dC) {
-  const int64_t per = Bsz * kN * L;  // elements of dB (and of dC)
+  const int64_t per = Bsz * NS * L;  // elements of dB (and of dC)
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= 2 * per) return;
-  const int64_t wh = i / per, e = i % per;  // e = (b * kN + n) * L + t
-  const int64_t b = e / (kN * L), nt = e % (kN * L);
+  const int64_t wh = i / per, e = i % per;  // e = (b * NS + n) * L + t
+  const int64_t b = e / (NS * L), nt = e % (NS * L);
   float acc = 0.f;
-  for (int64_t g = 0; g < nrb; ++g) acc += pBC[((b * nrb + g) * 2 + wh) * kN * L + nt];
+  for (int64_t g = 0; g < nrb; ++g) acc += pBC[((b * nrb + g) * 2 + wh) * NS * L + nt];
   (wh ? dC : dB)[e] = acc;
 }
 
@@ -708,20 +715,21 @@ __global__ void bwd_reduce_bc_kernel(const float* __restrict__ pBC, int64_t nrb,
 // batches g, g + 8, g + 16, ... (batch, then chunk order); the eight group
 // sums are then added in order of g.  Fixed order: bitwise reproducible.
 constexpr int kParamGroups = 8;
-__global__ void __launch_bounds__(kParamGroups * kN)
+template <int NS>
+__global__ void __launch_bounds__(kParamGroups * NS)
     bwd_reduce_param_kernel(const float* __restrict__ pA, const float* __restrict__ pD,
                             const float* __restrict__ pbias, int64_t Bsz, int64_t Dch,
                             int64_t nch, float* __restrict__ dA, float* __restrict__ dD,
                             float* __restrict__ dbias) {
-  __shared__ float sA[kParamGroups * kN], sD[kParamGroups], sB[kParamGroups];
+  __shared__ float sA[kParamGroups * NS], sD[kParamGroups], sB[kParamGroups];
   const int64_t d = blockIdx.x;
-  const int tid = threadIdx.x, n = tid % kN, gq = tid / kN;
+  const int tid = threadIdx.x, n = tid % NS, gq = tid / NS;
   float acc = 0.f, a1 = 0.f, a2 = 0.f;
   for (int64_t b = gq; b < Bsz; b += kParamGroups) {
     const int64_t rc0 = (b * Dch + d) * nch;
-    const float* src = pA + rc0 * kN + n;
+    const float* src = pA + rc0 * NS + n;
 #pragma unroll 8
-    for (int64_t c = 0; c < nch; ++c) acc += src[c * kN];
+    for (int64_t c = 0; c < nch; ++c) acc += src[c * NS];
     if (n == 0) {
 #pragma unroll 8
       for (int64_t c = 0; c < nch; ++c) {
@@ -736,11 +744,11 @@ __global__ void __launch_bounds__(kParamGroups * kN)
     sB[gq] = a2;
   }
   __syncthreads();
-  if (tid < kN) {
+  if (tid < NS) {
     float t = 0.f;
 #pragma unroll
-    for (int g = 0; g < kParamGroups; ++g) t += sA[g * kN + tid];
-    dA[d * kN + tid] = t;
+    for (int g = 0; g < kParamGroups; ++g) t += sA[g * NS + tid];
+    dA[d * NS + tid] = t;
   }
   if (tid == 0) {
     float t1 = 0.f, t2 = 0.f;
@@ -754,12 +762,12 @@ __global__ void __launch_bounds__(kParamGroups * kN)
   }
 }
 
-template <typename Io, bool kVec, int W, int kMinBlocks, int kSlotBufs>
+template <typename Io, bool kVec, int W, int kMinBlocks, int kSlotBufs, int NS>
 cudaError_t launch_main(const ScanArgs& a, const BwdOut& o, const WsLayout& w, float* sumS,
                         float* sumQ, float* pBC, float* pA, float* pD, float* pbias,
                         cudaStream_t s) {
-  using Sm = MainSmem<W, typename Io::T, kSlotBufs>;
-  auto kern = bwd_main_kernel<Io, kVec, W, kMinBlocks, kSlotBufs>;
+  using Sm = MainSmem<W, typename Io::T, kSlotBufs, NS>;
+  auto kern = bwd_main_kernel<Io, kVec, W, kMinBlocks, kSlotBufs, NS>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sm::total);
   if (e != cudaSuccess) return e;
@@ -768,9 +776,9 @@ cudaError_t launch_main(const ScanArgs& a, const BwdOut& o, const WsLayout& w, f
   return cudaGetLastError();
 }
 
-template <typename Io, bool kVec>
+template <typename Io, bool kVec, int NS>
 cudaError_t launch_bwd_t(int phase, const ScanArgs& a, const BwdOut& o, void* ws, cudaStream_t s) {
-  const WsLayout w = ws_layout(a.Bsz, a.Dch, a.L);
+  const WsLayout w = ws_layout(a.Bsz, a.Dch, a.L, NS);
   char* base = static_cast<char*>(ws);
   float* sumS = reinterpret_cast<float*>(base + w.sumS);
   float* sumQ = reinterpret_cast<float*>(base + w.sumQ);
@@ -781,53 +789,67 @@ cudaError_t launch_bwd_t(int phase, const ScanArgs& a, const BwdOut& o, void* ws
   float* pbias = reinterpret_cast<float*>(base + w.pbias);
   cudaError_t e;
   if (phase == 0) {
+    constexpr int SG = NS < 16 ? NS : 16;  // states per summary thread
     const int64_t nrb = (a.Dch + kSumThreads - 1) / kSumThreads;
-    dim3 grid((unsigned)(nrb * w.nchunks), (unsigned)a.Bsz);
-    const size_t smem = sizeof(float) * 2 * kBwdChunk * kN +
+    dim3 grid((unsigned)(nrb * w.nchunks), (unsigned)a.Bsz, (unsigned)(NS / SG));
+    const size_t smem = sizeof(float) * 2 * kBwdChunk * SG +
                         (kVec ? sizeof(uint4) * kSumDepth * 4 * (8 / Io::kVec) * kSumThreads : 0);
-    auto kern = bwd_summary_kernel<Io, kVec>;
+    auto kern = bwd_summary_kernel<Io, kVec, NS>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kSumThreads, smem, s>>>(a, o, nrb, sumS, sumQ, dsum);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const int64_t n = a.Bsz * a.Dch * kN;
-    bwd_carry_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a.A, a.Bsz, a.Dch, w.nchunks,
-                                                                 sumS, sumQ, dsum);
+    const int64_t n = a.Bsz * a.Dch * NS;
+    bwd_carry_kernel<NS><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a.A, a.Bsz, a.Dch,
+                                                                     w.nchunks, sumS, sumQ, dsum);
     return cudaGetLastError();
   }
   if (phase == 1) {
     // 4 warps per CTA, registers capped for three CTAs per SM (167 used, no
     // spills), one dB/dC slot buffer so that three CTAs also fit in shared
-    // memory: 12 warps per SM (measured fastest of 8/12 warps, 1/2 buffers)
-    return launch_main<Io, kVec, 4, 3, 1>(a, o, w, sumS, sumQ, pBC, pA, pD, pbias, s);
+    // memory with 16 states: 12 warps per SM (measured fastest of 8/12
+    // warps, 1/2 buffers).  Larger state sizes fit fewer CTAs per SM.
+    return launch_main<Io, kVec, 4, 3, 1, NS>(a, o, w, sumS, sumQ, pBC, pA, pD, pbias, s);
   }
-  const int64_t n = 2 * a.Bsz * kN * a.L;
-  bwd_reduce_bc_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(pBC, w.blocks, a.Bsz, a.L,
-                                                                     o.dB, o.dC);
+  const int64_t n = 2 * a.Bsz * NS * a.L;
+  bwd_reduce_bc_kernel<NS><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(pBC, w.blocks, a.Bsz,
+                                                                         a.L, o.dB, o.dC);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bwd_reduce_param_kernel<<<(unsigned)a.Dch, kParamGroups * kN, 0, s>>>(
+  bwd_reduce_param_kernel<NS><<<(unsigned)a.Dch, kParamGroups * NS, 0, s>>>(
       pA, pD, pbias, a.Bsz, a.Dch, w.nchunks, o.dA, o.dD, o.ddelta_bias);
   return cudaGetLastError();
 }
 
+template <typename Io, int NS>
+cudaError_t launch_bwd_ns(int phase, const ScanArgs& a, const BwdOut& o, void* ws,
+                          cudaStream_t s) {
+  return (a.L % Io::kVec) == 0 ? launch_bwd_t<Io, true, NS>(phase, a, o, ws, s)
+                               : launch_bwd_t<Io, false, NS>(phase, a, o, ws, s);
+}
+
+template <typename Io>
+cudaError_t launch_bwd_io(int phase, const ScanArgs& a, const BwdOut& o, void* ws,
+                          cudaStream_t s) {
+  switch (a.N) {
+    case 8: return launch_bwd_ns<Io, 8>(phase, a, o, ws, s);
+    case 16: return launch_bwd_ns<Io, 16>(phase, a, o, ws, s);
+    case 32: return launch_bwd_ns<Io, 32>(phase, a, o, ws, s);
+    case 64: return launch_bwd_ns<Io, 64>(phase, a, o, ws, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace
 
-size_t bwd_workspace_bytes(int64_t Bsz, int64_t Dch, int64_t L) {
-  return ws_layout(Bsz, Dch, L).total;
+size_t bwd_workspace_bytes(int64_t Bsz, int64_t Dch, int64_t L, int64_t N) {
+  return ws_layout(Bsz, Dch, L, N).total;
 }
 
 cudaError_t launch_scan_bwd(int phase, const ScanArgs& a, const BwdOut& o, void* ws,
                             cudaStream_t s) {
-  if (a.dt == Dt::BF16) {
-    return (a.L % IoBf16::kVec) == 0 ? launch_bwd_t<IoBf16, true>(phase, a, o, ws, s)
-                                     : launch_bwd_t<IoBf16, false>(phase, a, o, ws, s);
-  }
-  if (a.dt == Dt::F16) {
-    return (a.L % IoF16::kVec) == 0 ? launch_bwd_t<IoF16, true>(phase, a, o, ws, s)
-                                    : launch_bwd_t<IoF16, false>(phase, a, o, ws, s);
-  }
-  return (a.L % IoF32::kVec) == 0 ? launch_bwd_t<IoF32, true>(phase, a, o, ws, s)
-                                  : launch_bwd_t<IoF32, false>(phase, a, o, ws, s);
+  if (a.dt == Dt::BF16) return launch_bwd_io<IoBf16>(phase, a, o, ws, s);
+  if (a.dt == Dt::F16) return launch_bwd_io<IoF16>(phase, a, o, ws, s);
+  return launch_bwd_io<IoF32>(phase, a, o, ws, s);
 }
 
 }  // namespace selscan

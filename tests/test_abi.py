@@ -85,7 +85,8 @@ def test_workspace_size():
     big = n.value
     assert f(8, 2048, 4096, 16, 0, ctypes.byref(n)) == OK and n.value > big
     assert f(0, 2048, 2048, 16, 0, ctypes.byref(n)) == OK and n.value == 0
-    assert f(8, 2048, 2048, 8, 0, ctypes.byref(n)) == NUNS
+    assert f(8, 2048, 2048, 12, 0, ctypes.byref(n)) == NUNS
+    assert f(8, 2048, 2048, 64, 0, ctypes.byref(n)) == OK and n.value > big
     assert f(8, 2048, 2048, 16, 9, ctypes.byref(n)) == DTYPE
     assert f(8, 2048, 2048, 16, 0, None) == NULL
     assert ss.ss_scan_bwd_workspace_size(2, 16, 64) % 256 == 0
@@ -105,7 +106,7 @@ def bwd(**kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(dtype=5), DTYPE),
     (dict(N=4), NUNS),
-    (dict(N=32), NUNS),             # the backward takes N = 16 only
+    (dict(N=48), NUNS),
     (dict(L=-5), SHAPE),
     (dict(dy=None), NULL),
     (dict(dB=None), NULL),

@@ -1,15 +1,15 @@
-"""State sizes other than 16 (d_state = 8, 32, 64): the forward scans (the
-row-sequential kernel, 16-byte and element-wise rows) and the one-token step
-on the GPU against the fp64 oracle.  The backward takes N = 16 only and
-rejects the others before launching anything."""
+"""State sizes other than 16 (d_state = 8, 32, 64) on the GPU against the
+fp64 oracle: the forward scans (the row-sequential kernel, 16-byte and
+element-wise rows), the backward (the chunk-parallel kernels with state
+groups) and the one-token step."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import synth
-from parity_util import (as_io, check, inputs_to_dev, make_case, oracle_fwd, out_kind, to_dev,
-                         to_host64)
+from parity_util import (as_io, check, grad_kind, inputs_to_dev, make_case, oracle_bwd, oracle_fwd,
+                         out_kind, to_dev, to_host64)
 
 import selective_state_space_114_b300 as ss
 
@@ -130,11 +130,52 @@ def test_scan_then_step_equals_longer_scan(N):
     check(to_host64(h), href, "bf16", f"N={N} state after steps")
 
 
+IO_GRADS = ("du", "ddelta", "dz")
+F32_GRADS = ("dA", "dB", "dC", "dD", "ddelta_bias")
+
+
+def compare_bwd(x, dtype, what, softplus=True):
+    dy = x.pop("dy")
+    xd = inputs_to_dev(x, dtype)
+    g = ss.ss_scan_bwd(xd["u"], xd["delta"], xd["A"], xd["B"], xd["C"], xd.get("D"), xd.get("z"),
+                       xd.get("delta_bias"), softplus, to_dev(dy, dtype))
+    torch.cuda.synchronize()
+    ref = oracle_bwd(x, dy, softplus)
+    for k in IO_GRADS + F32_GRADS:
+        if ref[k] is None:
+            assert g[k] is None, k
+            continue
+        check(to_host64(g[k]), ref[k], grad_kind(dtype, k in IO_GRADS), f"{what} {k}")
+
+
 @pytest.mark.parametrize("N", NS)
-def test_backward_rejects_other_state_sizes(N):
-    x = make_case("f32", 1, 8, 16, seed=3, N=N, with_dy=True)
-    xd = inputs_to_dev(x, "f32")
-    with pytest.raises(ss.SelscanError) as e:
-        ss.ss_scan_bwd(xd["u"], xd["delta"], xd["A"], xd["B"], xd["C"], xd["D"], xd["z"],
-                       xd["delta_bias"], True, xd["dy"])
-    assert e.value.status == 4
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("Bsz,Dch,L", [
+    (2, 20, 300),   # several 128-step chunks, a ragged last chunk
+    (1, 130, 136),  # two 128-row blocks, element-wise rows for 16-bit I/O
+    (2, 9, 37),     # element-wise rows
+])
+def test_backward(N, dtype, Bsz, Dch, L):
+    x = make_case(dtype, Bsz, Dch, L, seed=700 + N + L, with_dy=True, N=N)
+    compare_bwd(x, dtype, f"N={N} {dtype} {Bsz}x{Dch}x{L}")
+
+
+@pytest.mark.parametrize("N", NS)
+def test_backward_optional_inputs_and_no_softplus(N):
+    x = make_case("f32", 2, 18, 200, seed=80 + N, with_dy=True, N=N)
+    x.update(D=None, z=None, delta_bias=None)
+    x["delta"] = as_io(np.abs(synth.widen(x["delta"])) * 0.05, "f32")
+    compare_bwd(x, "f32", f"N={N} no D, z, bias, softplus", softplus=False)
+
+
+@pytest.mark.parametrize("N", NS)
+def test_backward_deterministic(N):
+    x = make_case("bf16", 2, 40, 400, seed=5, with_dy=True, N=N)
+    dy = to_dev(x.pop("dy"), "bf16")
+    xd = inputs_to_dev(x, "bf16")
+    args = (xd["u"], xd["delta"], xd["A"], xd["B"], xd["C"], xd["D"], xd["z"], xd["delta_bias"],
+            True, dy)
+    g1, g2 = ss.ss_scan_bwd(*args), ss.ss_scan_bwd(*args)
+    torch.cuda.synchronize()
+    for k, v in g1.items():
+        assert torch.equal(v, g2[k]), k
