@@ -564,6 +564,63 @@ def configs_measure(ss, dev, seed):
                                                "resource")}}
     del x, y, h
     torch.cuda.empty_cache()
+
+    # the bench layer (8 x 1536 x 2048, bf16) with 64 states, forward and backward
+    cfg = dict(synth.config(1), N=64)
+    x, dtype = _device_inputs(cfg, dev, seed + 5, with_dy=True)
+    Bsz, Dch, L, N = cfg["Bsz"], cfg["Dch"], cfg["L"], cfg["N"]
+    E = Bsz * Dch * L
+    y = torch.empty_like(x["u"])
+    ws = torch.empty(ss.ss_scan_bwd_workspace_size(Bsz, Dch, L, N, ss.SS_BF16), device=dev,
+                     dtype=torch.uint8)
+    args = (x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], True)
+    g = ss.ss_scan_bwd(*args, x["dy"], workspace=ws)
+    fns = [lambda: ss.ss_scan_fwd(*args, out=y)]
+    for st in ("ss_scan_bwd_states", "ss_scan_bwd_reverse", "ss_scan_bwd_reduce"):
+        fns.append(lambda st=st: ss.ss_scan_bwd(*args, x["dy"], workspace=ws, out=g,
+                                                stages=(st,)))
+    ms = _timed_ms(fns, 5, dev)
+    work = kernel_work(2, Dch, N)
+    out["state_size_64_bf16_fwd_bwd"] = {
+        "workload": f"Bsz={Bsz} Dch={Dch} L={L} N={N}, bf16 I/O, fwd + bwd, inputs larger than L2",
+        "gelem_s": round(E / (sum(ms) * 1e-3) / 1e9, 3), "ms": round(sum(ms), 4),
+        "kernels": {nm: {"ms": round(t, 4), **{k: v for k, v in roofline(nm, work[nm], E, t, hbm)
+                                               .items() if k in ("bound", "achieved", "peak",
+                                                                 "unit", "frac", "resource")}}
+                    for nm, t in zip(["fwd", "bwd_states", "bwd_reverse", "bwd_reduce"], ms)}}
+    del x, y, g, ws
+    torch.cuda.empty_cache()
+
+    # chunked prefill: the bench layer's forward as four 512-step pieces, each
+    # continuing from the state the previous one left (updated in place)
+    cfg = synth.config(1)
+    x, dtype = _device_inputs(cfg, dev, seed + 6)
+    Bsz, Dch, L, N = cfg["Bsz"], cfg["Dch"], cfg["L"], cfg["N"]
+    E = Bsz * Dch * L
+    P = 4
+    Lp = L // P
+    pieces = [{k: x[k][..., i * Lp:(i + 1) * Lp].contiguous() for k in ("u", "delta", "z", "B",
+                                                                       "C")}
+              for i in range(P)]
+    ys = [torch.empty_like(pc["u"]) for pc in pieces]
+    h = torch.zeros((Bsz, Dch, N), device=dev)
+
+    def prefill():
+        for i, pc in enumerate(pieces):
+            ss.ss_scan_fwd(pc["u"], pc["delta"], x["A"], pc["B"], pc["C"], x["D"], pc["z"],
+                           x["delta_bias"], True, out=ys[i], return_last_state=True,
+                           h0=h if i else None, h_last=h)
+
+    (t,) = _timed_ms([prefill], 10, dev)
+    r = roofline("fwd", kernel_work(2, Dch)["fwd"], E, t, hbm)
+    out["chunked_prefill_bf16_fwd"] = {
+        "workload": f"Bsz={Bsz} Dch={Dch} L={L} N={N} as {P} pieces of {Lp} steps continued "
+                    f"from the carried state (ss_scan_fwd_from_state), bf16 I/O",
+        "gelem_s": round(E / (t * 1e-3) / 1e9, 3), "ms": round(t, 4),
+        **{k: v for k, v in r.items() if k in ("bound", "achieved", "peak", "unit", "frac",
+                                               "resource")}}
+    del x, pieces, ys, h
+    torch.cuda.empty_cache()
     return out
 
 

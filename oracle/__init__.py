@@ -77,6 +77,7 @@ class Oracle:
         l.oracle_step.argtypes = [p] * 9 + [ci, i64, i64, i64, p, ci]
         l.oracle_conv1d_silu.argtypes = [p] * 3 + [ci, i64, i64, i64, i64, p, ci]
         l.oracle_conv1d_silu_bwd.argtypes = [p] * 3 + [ci, p, i64, i64, i64, i64, p, p, p, ci]
+        l.oracle_xproj.argtypes = [p] * 3 + [i64] * 5 + [p] * 3 + [ci]
         for f in (l.oracle_scan_fwd, l.oracle_scan_fwd_blelloch, l.oracle_scan_bwd, l.oracle_step):
             f.restype = ci
         self._l = l
@@ -182,6 +183,23 @@ class Oracle:
             raise RuntimeError(f"oracle conv1d_silu_bwd failed ({rc})")
         return out
 
+    def xproj(self, u, Wx, Wdt, N, nthreads=None):
+        """Input projection (x_proj then dt_proj): u [Bsz][Dch][L], Wx [R+2N][Dch],
+        Wdt [Dch][R] -> (delta_raw [Bsz][Dch][L], B [Bsz][N][L], C [Bsz][N][L])."""
+        u = _f64(u)
+        Bsz, Dch, L = u.shape
+        Wdt = _f64(Wdt)
+        R = Wdt.shape[1]
+        Wx = _f64(Wx, (R + 2 * N, Dch))
+        delta = np.zeros((Bsz, Dch, L))
+        B = np.zeros((Bsz, N, L))
+        C = np.zeros((Bsz, N, L))
+        rc = self._l.oracle_xproj(_p(u), _p(Wx), _p(Wdt), Bsz, Dch, L, R, N, _p(delta), _p(B),
+                                   _p(C), nthreads or default_threads())
+        if rc:
+            raise ValueError("oracle_xproj: bad arguments")
+        return delta, B, C
+
 
 def default() -> Oracle:
     global _default
@@ -209,3 +227,7 @@ def conv1d_silu(*a, **k):
 
 def conv1d_silu_bwd(*a, **k):
     return default().conv1d_silu_bwd(*a, **k)
+
+
+def xproj(*a, **k):
+    return default().xproj(*a, **k)

@@ -533,3 +533,57 @@ int oracle_conv1d_silu_bwd(const double* x, const double* w, const double* bias,
     run_rows(conv_bwd_channel, &c, Dch, nthreads);
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* input projection: x_proj then dt_proj, producing delta_raw, B, C    */
+/* ------------------------------------------------------------------ */
+/*
+ * The projections that feed the scan ("PyTorch 한 파일에서의 Mamba 구현",
+ * news.hada.io topic 12448, and its Vietnamese edition, comment thread:
+ * x_proj has no bias, so x_proj and dt_proj compose into one projection and
+ * dt_proj's bias is the one the scan adds to delta_raw).  With R = dt_rank,
+ * N states and M = R + 2N projected features per token:
+ *
+ *   xdbl[b][t][m]  = sum_{k < Dch} Wx[m][k] u[b][k][t]          (m < M)
+ *   delta[b][d][t] = sum_{r < R}   Wdt[d][r] xdbl[b][t][r]
+ *   B[b][n][t]     = xdbl[b][t][R + n],   C[b][n][t] = xdbl[b][t][R + N + n]
+ *
+ * Layouts: u, delta [Bsz][Dch][L]; Wx [M][Dch]; Wdt [Dch][R]; B, C [Bsz][N][L].
+ * One job per (b, t) token.
+ */
+typedef struct {
+    const double *u, *Wx, *Wdt;
+    i64 Bsz, Dch, L, R, N;
+    double *delta, *B, *C;
+} xproj_ctx;
+
+static void xproj_token(void* p, i64 bt, int tid) {
+    (void)tid;
+    const xproj_ctx* c = (const xproj_ctx*)p;
+    const i64 b = bt / c->L, t = bt % c->L, M = c->R + 2 * c->N;
+    const double* ub = c->u + b * c->Dch * c->L;
+    double* x = (double*)malloc(sizeof(double) * (size_t)(M > 0 ? M : 1));
+    for (i64 m = 0; m < M; ++m) {
+        double s = 0.0;
+        for (i64 k = 0; k < c->Dch; ++k) s += c->Wx[m * c->Dch + k] * ub[k * c->L + t];
+        x[m] = s;
+    }
+    for (i64 d = 0; d < c->Dch; ++d) {
+        double s = 0.0;
+        for (i64 r = 0; r < c->R; ++r) s += c->Wdt[d * c->R + r] * x[r];
+        c->delta[(b * c->Dch + d) * c->L + t] = s;
+    }
+    for (i64 n = 0; n < c->N; ++n) {
+        c->B[(b * c->N + n) * c->L + t] = x[c->R + n];
+        c->C[(b * c->N + n) * c->L + t] = x[c->R + c->N + n];
+    }
+    free(x);
+}
+
+int oracle_xproj(const double* u, const double* Wx, const double* Wdt, i64 Bsz, i64 Dch, i64 L,
+                 i64 R, i64 N, double* delta, double* B, double* C, int nthreads) {
+    if (Bsz < 0 || Dch < 0 || L < 0 || R < 0 || N < 0) return 1;
+    xproj_ctx c = {u, Wx, Wdt, Bsz, Dch, L, R, N, delta, B, C};
+    run_rows(xproj_token, &c, Bsz * L, nthreads);
+    return 0;
+}

@@ -325,7 +325,44 @@ def pin_conv_bwd_fd(orc, seed=15):
         _close(got[name], num, 1e-6, 1e-7, f"conv finite differences {name}")
 
 
+def pin_xproj_one_hot(orc, seed=16):
+    """One-hot projection weights pick channels: every output is a copy of one
+    input channel (pins which weight index is the feature and which the
+    channel, the split of xdbl into the dt part, B and C, and the dt_proj
+    contraction index)."""
+    rng = np.random.default_rng(seed)
+    Bsz, Dch, L, R, N = 2, 7, 5, 2, 3
+    M = R + 2 * N
+    u = rng.standard_normal((Bsz, Dch, L))
+    pick = rng.integers(Dch, size=M)          # feature m <- channel pick[m]
+    Wx = np.zeros((M, Dch))
+    Wx[np.arange(M), pick] = 1.0
+    via = rng.integers(R, size=Dch)           # delta channel d <- dt feature via[d]
+    Wdt = np.zeros((Dch, R))
+    Wdt[np.arange(Dch), via] = 1.0
+    delta, B, C = orc.xproj(u, Wx, Wdt, N, nthreads=1)
+    _close(delta, u[:, pick[via], :], 0, 0, "xproj one-hot delta")
+    _close(B, u[:, pick[R:R + N], :], 0, 0, "xproj one-hot B")
+    _close(C, u[:, pick[R + N:], :], 0, 0, "xproj one-hot C")
+
+
+def pin_xproj_merged_weights(orc, seed=17):
+    """The pages' observation: with no bias in x_proj, x_proj then dt_proj is
+    one projection by the merged weight Wdt Wx[:R] (numpy matmuls in the
+    merged association order)."""
+    rng = np.random.default_rng(seed)
+    Bsz, Dch, L, R, N = 2, 12, 9, 4, 3
+    u = rng.standard_normal((Bsz, Dch, L))
+    Wx = rng.standard_normal((R + 2 * N, Dch))
+    Wdt = rng.standard_normal((Dch, R))
+    delta, B, C = orc.xproj(u, Wx, Wdt, N, nthreads=2)
+    merged = Wdt @ Wx[:R]
+    _close(delta, np.matmul(merged, u), 0, 1e-12, "xproj merged delta")
+    _close(B, np.matmul(Wx[R:R + N], u), 0, 1e-12, "xproj B")
+    _close(C, np.matmul(Wx[R + N:], u), 0, 1e-12, "xproj C")
+
+
 ALL_PINS = [pin_closed_form, pin_delta_zero, pin_geometric, pin_lfilter, pin_softplus_cumsum,
             pin_gate_order, pin_blelloch, pin_resume, pin_scan_then_step, pin_bwd_fd,
             pin_bwd_fd_plain, pin_conv_convolve, pin_conv_lfilter, pin_conv_impulse,
-            pin_conv_bwd_fd]
+            pin_conv_bwd_fd, pin_xproj_one_hot, pin_xproj_merged_weights]

@@ -49,6 +49,12 @@ MUTANTS = [
      "if (t < L) acc += c->w[d * K + (K - 1 - k)] * gc[t];"),
     ("conv_dw_wrong_shift", "if (src >= 0) c->dw[d * K + k] += gc[t] * xr[src];",
      "if (src >= 1) c->dw[d * K + k] += gc[t] * xr[src - 1];"),
+    ("xproj_weight_transposed", "s += c->Wx[m * c->Dch + k] * ub[k * c->L + t];",
+     "s += c->Wx[(k % M) * c->Dch + (m % c->Dch)] * ub[k * c->L + t];"),
+    ("xproj_B_C_swapped", "c->B[(b * c->N + n) * c->L + t] = x[c->R + n];",
+     "c->B[(b * c->N + n) * c->L + t] = x[c->R + c->N + n];"),
+    ("xproj_dt_part_shifted", "for (i64 r = 0; r < c->R; ++r) s += c->Wdt[d * c->R + r] * x[r];",
+     "for (i64 r = 0; r < c->R; ++r) s += c->Wdt[d * c->R + r] * x[r + 1];"),
 ]
 
 
