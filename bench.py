@@ -431,6 +431,35 @@ def conv_measure(ss, dev, seed, steps=16):
                      "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(ach / hbm, 4), "algorithmic_bytes": nbytes}
     return res
+def xproj_measure(ss, dev, seed, steps=16):
+    """The input projection (x_proj then dt_proj on the tensor cores) on the
+    bench layer's shape (8 x 1536 x 2048, dt_rank 48, N = 16, bf16), L2
+    flushed before each call.  HBM-bound: u read, delta, B, C written."""
+    import torch
+    cfg = synth.config(CFG_INDEX)
+    Bsz, Dch, L, N, R = cfg["Bsz"], cfg["Dch"], cfg["L"], cfg["N"], 48
+    E = Bsz * Dch * L
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    bf = torch.bfloat16
+    u = torch.randn((Bsz, Dch, L), generator=gen, device=dev).to(bf)
+    Wx = (torch.randn((R + 2 * N, Dch), generator=gen, device=dev) / Dch ** 0.5).to(bf)
+    Wdt = (torch.randn((Dch, R), generator=gen, device=dev) / R ** 0.5).to(bf)
+    out = (torch.empty_like(u), torch.empty((Bsz, N, L), device=dev, dtype=bf),
+           torch.empty((Bsz, N, L), device=dev, dtype=bf))
+    ms = _flushed_median_ms(lambda: ss.ss_xproj(u, Wx, Wdt, N, out=out), steps, dev)
+    nbytes = 2 * E * 2 + 2 * 2 * Bsz * N * L + 2 * (R + 2 * N) * Dch + 2 * Dch * R
+    flops = 2 * Bsz * L * Dch * (R + 2 * N) + 2 * Bsz * L * R * Dch
+    hbm, _ = load_peaks()
+    ach = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"x_proj + dt_proj, Bsz={Bsz} Dch={Dch} L={L} dt_rank={R} N={N}, bf16, "
+                        f"L2 flushed before each call",
+            "ms": round(ms, 4), "bound": "hbm", "achieved": round(ach, 1), "peak": hbm,
+            "unit": "GB/s", "frac": round(ach / hbm, 4), "algorithmic_bytes": nbytes,
+            "tensor_tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+            "wait_failures": ss.ss_xproj_wait_failures()}
+
+
 def decode_step_measure(ss, dev, seed, steps=16):
     """The one-token step on the decode workload (Bsz=256, Dch=5120, N=16,
     bf16 tokens, float32 state): its state (84 MB) fits in L2, so L2 is
@@ -750,6 +779,7 @@ def run_ours(args):
     decode = decode_step_measure(ss, dev, seed) if rank == 0 else None
     conv = conv_measure(ss, dev, seed) if rank == 0 else None
     others = configs_measure(ss, dev, seed) if rank == 0 else None
+    xproj = xproj_measure(ss, dev, seed) if rank == 0 else None
 
     # end to end through the public API with host buffers
     Ke = max(3, min(K, 10))
@@ -797,6 +827,7 @@ def run_ours(args):
         "decode_step": decode,
         "conv1d_silu": conv,
         "other_workloads": others,
+        "xproj": xproj,
         "e2e": {"value": round(world * E / (e2e_ms * 1e-3) / 1e9, 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 3)},

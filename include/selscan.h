@@ -226,6 +226,35 @@ ss_status ss_conv1d_silu_bwd(const void* x, const float* w, const float* bias, i
                              ss_stream_t stream);
 
 /*
+ * Input projection that produces the scan's delta_raw, B and C from u
+ * (x_proj, which has no bias, then dt_proj without its bias, which the scan
+ * adds as delta_bias; "PyTorch 한 파일에서의 Mamba 구현", news.hada.io topic
+ * 12448, comment thread on merging the two projections).  Per batch b, with
+ * R = dt_rank and N states:
+ *   xdbl[t][m]     = sum_k Wx[m][k] u[b][k][t]        (m < R + 2N)
+ *   delta[b][d][t] = sum_r Wdt[d][r] xdbl[t][r]       (r < R)
+ *   B[b][n][t] = xdbl[t][R + n],  C[b][n][t] = xdbl[t][R + N + n]
+ *   in : u [Bsz][Dch][L]; Wx [R + 2N][Dch]; Wdt [Dch][R]; all SS_BF16 or all
+ *        SS_F16 (SS_ERR_DTYPE otherwise); fp32 accumulation on the tensor
+ *        cores; xdbl[.][r < R] is rounded to the I/O type before dt_proj.
+ *   out: delta [Bsz][Dch][L]; B, C [Bsz][N][L] (I/O dtype).
+ * Shapes: L, Dch and R multiples of 8, R >= 8, N >= 1, R + 2N <= 256
+ * (SS_ERR_SHAPE otherwise).  Outputs must not overlap the inputs.
+ * Conventions as for the scan (device pointers, 16-byte alignment, async on
+ * stream, checks before launch).
+ */
+ss_status ss_xproj(const void* u, const void* Wx, const void* Wdt, int64_t Bsz, int64_t Dch,
+                   int64_t L, int64_t R, int64_t N, ss_dtype dtype, void* delta, void* B, void* C,
+                   ss_stream_t stream);
+
+/*
+ * Number of ss_xproj CTAs (since the library was loaded) whose bounded wait
+ * for the tensor cores gave up; such a CTA leaves its outputs incomplete.
+ * Synchronous (device-to-host copy on the legacy stream); -1 on a CUDA error.
+ */
+int ss_xproj_wait_failures(void);
+
+/*
  * Backward scan for callers that cannot allocate device memory.
  *
  * The pages describe no counterpart of this entry point; it exists for

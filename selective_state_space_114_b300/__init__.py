@@ -69,6 +69,10 @@ def _load() -> ctypes.CDLL:
         f.restype = ci
     lib.ss_step.argtypes = [p] * 9 + [ci, i64, i64, i64, ci, p, p]
     lib.ss_step.restype = ci
+    lib.ss_xproj.argtypes = [p] * 3 + [i64] * 5 + [ci] + [p] * 4
+    lib.ss_xproj.restype = ci
+    lib.ss_xproj_wait_failures.argtypes = []
+    lib.ss_xproj_wait_failures.restype = ci
     lib.ss_conv1d_silu_fwd.argtypes = [p, p, p, ci, i64, i64, i64, i64, ci, p, p]
     lib.ss_conv1d_silu_fwd.restype = ci
     lib.ss_conv1d_silu_bwd.argtypes = [p, p, p, ci, p, i64, i64, i64, i64, ci, p, p, p, p]
@@ -86,7 +90,7 @@ EXPORTED_SYMBOLS = ("ss_status_str", "ss_version", "ss_scan_fwd", "ss_scan_fwd_f
                     "ss_scan_bwd", "ss_scan_bwd_states", "ss_scan_bwd_reverse",
                     "ss_scan_bwd_reduce", "ss_step", "ss_conv1d_silu_fwd",
                     "ss_conv1d_silu_bwd", "ss_scan_bwd_noalloc",
-                    "ss_scan_bwd_noalloc_max_scratch")
+                    "ss_scan_bwd_noalloc_max_scratch", "ss_xproj", "ss_xproj_wait_failures")
 
 
 def lib() -> ctypes.CDLL:
@@ -303,3 +307,25 @@ def ss_conv1d_silu_bwd(x, w, bias, silu, du, out=None):
                                    Dch, L, K, _dtype_code(x), _ptr(g["dx"]), _ptr(g["dw"]),
                                    _ptr(g["dbias"]), _stream(x.device)))
     return g
+
+
+def ss_xproj(u, Wx, Wdt, N, out=None):
+    """Input projection (x_proj then dt_proj, on the tensor cores): u
+    [Bsz][Dch][L], Wx [R + 2N][Dch], Wdt [Dch][R], all bf16 or all fp16.
+    Returns (delta_raw [Bsz][Dch][L], B [Bsz][N][L], C [Bsz][N][L])."""
+    Bsz, Dch, L = u.shape
+    R = Wdt.shape[1]
+    _same(Wx, (R + 2 * N, Dch), u.dtype, "Wx")
+    _same(Wdt, (Dch, R), u.dtype, "Wdt")
+    if out is None:
+        out = (torch.empty_like(u), torch.empty((Bsz, N, L), device=u.device, dtype=u.dtype),
+               torch.empty((Bsz, N, L), device=u.device, dtype=u.dtype))
+    delta, B, C = out
+    _check("ss_xproj", _lib.ss_xproj(_ptr(u), _ptr(Wx), _ptr(Wdt), Bsz, Dch, L, R, N,
+                                     _dtype_code(u), _ptr(delta), _ptr(B), _ptr(C),
+                                     _stream(u.device)))
+    return delta, B, C
+
+
+def ss_xproj_wait_failures() -> int:
+    return int(_lib.ss_xproj_wait_failures())

@@ -272,4 +272,28 @@ ss_status ss_conv1d_silu_bwd(const void* x, const float* w, const float* bias, i
   return cuda_status(selscan::launch_conv(1, a, o, s));
 }
 
+ss_status ss_xproj(const void* u, const void* Wx, const void* Wdt, int64_t Bsz, int64_t Dch,
+                   int64_t L, int64_t R, int64_t N, ss_dtype dtype, void* delta, void* B, void* C,
+                   ss_stream_t stream) {
+  if (dtype != SS_BF16 && dtype != SS_F16) return SS_ERR_DTYPE;
+  if (bad_size(Bsz) || bad_size(Dch) || bad_size(L) || bad_size(R) || bad_size(N))
+    return SS_ERR_SHAPE;
+  if (product_too_big(Bsz, Dch, L) || R < 8 || R % 8 || N < 1 || R + 2 * N > 256 || Dch % 8 ||
+      L % 8 || Bsz * ((L + 127) / 128) > 0x7fffffff)
+    return SS_ERR_SHAPE;
+  const bool work = Bsz > 0 && Dch > 0 && L > 0;
+  if (work && (!u || !Wx || !Wdt || !delta || !B || !C)) return SS_ERR_NULL;
+  if (misaligned(u) || misaligned(Wx) || misaligned(Wdt) || misaligned(delta) || misaligned(B) ||
+      misaligned(C))
+    return SS_ERR_ALIGN;
+  if (!work) return SS_OK;
+  selscan::XprojArgs a{u, Wx, Wdt, Bsz, Dch, L, R, N, to_dt(dtype), delta, B, C};
+  return cuda_status(selscan::launch_xproj(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int ss_xproj_wait_failures(void) {
+  int n = 0;
+  return selscan::xproj_wait_failures(&n) == cudaSuccess ? n : -1;
+}
+
 }  // extern "C"

@@ -89,4 +89,21 @@ struct ConvGrads {
 // backward (writes o.dx, o.dw, o.dbias).  Requires Bsz*Dch*L > 0.
 cudaError_t launch_conv(int phase, const ConvArgs& a, const ConvGrads& o, cudaStream_t s);
 
+struct XprojArgs {
+  const void* u;    // [Bsz][Dch][L]
+  const void* Wx;   // [R + 2N][Dch]
+  const void* Wdt;  // [Dch][R]
+  int64_t Bsz, Dch, L, R, N;
+  Dt dt;            // BF16 or F16
+  void* delta;      // [Bsz][Dch][L]
+  void* B;          // [Bsz][N][L]
+  void* C;          // [Bsz][N][L]
+};
+
+// Input projection (x_proj then dt_proj) on the tensor cores.  Requires
+// Bsz*Dch*L > 0, L, Dch, R multiples of 8, R >= 8, N >= 1, R + 2N <= 256.
+cudaError_t launch_xproj(const XprojArgs& a, cudaStream_t s);
+size_t xproj_smem_bytes(int64_t R, int64_t N);
+cudaError_t xproj_wait_failures(int* out);
+
 }  // namespace selscan

@@ -203,3 +203,24 @@ def test_conv_bwd_rejects(kw, code):
 
 def test_conv_empty_forward_is_ok_without_pointers():
     assert conv(x=None, w=None, u=None, L=0) == OK
+
+
+def xproj(**kw):
+    a = dict(u=P, Wx=P, Wdt=P, Bsz=2, Dch=64, L=128, R=16, N=8, dtype=1, delta=P, B=P, C=P)
+    a.update(kw)
+    return ss.lib().ss_xproj(a["u"], a["Wx"], a["Wdt"], a["Bsz"], a["Dch"], a["L"], a["R"], a["N"],
+                             a["dtype"], a["delta"], a["B"], a["C"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=0), DTYPE), (dict(dtype=7), DTYPE), (dict(R=4), SHAPE), (dict(R=12), SHAPE),
+    (dict(N=0), SHAPE), (dict(R=160, N=56), SHAPE), (dict(L=100), SHAPE), (dict(Dch=60), SHAPE),
+    (dict(L=-8), SHAPE), (dict(u=None), NULL), (dict(C=None), NULL), (dict(Wx=MIS), ALIGN),
+    (dict(delta=MIS), ALIGN),
+])
+def test_xproj_rejects(kw, code):
+    assert xproj(**kw) == code
+
+
+def test_xproj_empty_is_ok_without_pointers():
+    assert xproj(u=None, Wx=None, Wdt=None, delta=None, B=None, C=None, L=0) == OK
