@@ -34,6 +34,8 @@
 //            (row, chunk).
 //  stage 2   bwd_reduce: fixed-order sums of the partials (results are
 //            bitwise reproducible).
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -342,7 +344,7 @@ __device__ __forceinline__ int slot_swizzle(int j) { return 2 * ((j >> 1) & 1); 
 // (pre-gate output, sum lam B, sum A lam a h) in the row's registers, stores
 // the row's dB and dC terms of the pair at dB_lo / dC_lo (state 2q, state 2q+1
 // at +CH) and the lane's dA terms of the two states at dA_lo[0], dA_lo[RL].
-template <int KT, int RL, int CH, int NS>
+template <int KT, int RL, int CH, int NS, bool kKeepB>
 __device__ __forceinline__ void bwd_state_pair(
     int q, int j, int r, bool valid, const float* A2s, const float* Ars, const float* hin_row,
     const float* rin_row, const float4* Bp, const float4* Cp, const float (&dl)[KT],
@@ -356,6 +358,13 @@ __device__ __forceinline__ void bwd_state_pair(
     const float4* cq = Cp + q * (KT / 2) * RL + j;
 
     float2 a[KT], bb[KT], mu[KT];
+    // kKeepB: the lane's B steps stay in registers from the prep to the
+    // reverse replay (one shared-memory read instead of two)
+    float4 Bk[KT / 2];
+    if (kKeepB) {
+#pragma unroll
+      for (int k = 0; k < KT / 2; ++k) Bk[k] = bq[k * RL];
+    }
 #pragma unroll
     for (int k = 0; k < KT / 2; ++k) {
       const float2 dd = make_float2(dl[2 * k], dl[2 * k + 1]);
@@ -363,7 +372,7 @@ __device__ __forceinline__ void bwd_state_pair(
       const float2 e1 = mul2(dd, make_float2(a2.y, a2.y));
       a[2 * k] = make_float2(ex2f(e0.x), ex2f(e1.x));
       a[2 * k + 1] = make_float2(ex2f(e0.y), ex2f(e1.y));
-      const float4 v = bq[k * RL];
+      const float4 v = kKeepB ? Bk[k] : bq[k * RL];
       bb[2 * k] = mul2(du2[2 * k], make_float2(v.x, v.y));
       bb[2 * k + 1] = mul2(du2[2 * k + 1], make_float2(v.z, v.w));
       const float4 cv = cq[k * RL];
@@ -435,7 +444,7 @@ __device__ __forceinline__ void bwd_state_pair(
     float2 dA2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = KT / 2 - 1; k >= 0; --k) {
-      const float4 bv = bq[k * RL];
+      const float4 bv = kKeepB ? Bk[k] : bq[k * RL];
 #pragma unroll
       for (int e = 1; e >= 0; --e) {
         const int i = 2 * k + e;
@@ -454,7 +463,7 @@ __device__ __forceinline__ void bwd_state_pair(
 
 }
 
-template <typename Io, bool kVec, int W, int kMinBlocks, int kSlotBufs, int NS>
+template <typename Io, bool kVec, int W, int kMinBlocks, int kSlotBufs, int NS, bool kKeepB>
 __global__ void __launch_bounds__(W * 32, kMinBlocks)
     bwd_main_kernel(ScanArgs p, BwdOut o, int64_t nrb, const float* __restrict__ Hin,
                     const float* __restrict__ Rin, float* __restrict__ pBC,
@@ -600,7 +609,7 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks)
     for (int q = 0; q < NS / 2; ++q) {
       const int sb = kSlotBufs == 2 ? (q & 1) : 0;
       float* slot = my_slot0 + (size_t)sb * R * SR;
-      bwd_state_pair<KT, RL, CH, NS>(q, j, r, valid, A2s, Ars, hin_row, rin_row, Bp, Cp, dl, du2,
+      bwd_state_pair<KT, RL, CH, NS, kKeepB>(q, j, r, valid, A2s, Ars, hin_row, rin_row, Bp, Cp, dl, du2,
                                      yh2, dsum, yacc2, s12, s22, slot, slot + 2 * CH,
                                      dAs + (r * NS + 2 * q) * RL + j);
 
@@ -762,12 +771,12 @@ __global__ void __launch_bounds__(kParamGroups * NS)
   }
 }
 
-template <typename Io, bool kVec, int W, int kMinBlocks, int kSlotBufs, int NS>
+template <typename Io, bool kVec, int W, int kMinBlocks, int kSlotBufs, int NS, bool kKeepB>
 cudaError_t launch_main(const ScanArgs& a, const BwdOut& o, const WsLayout& w, float* sumS,
                         float* sumQ, float* pBC, float* pA, float* pD, float* pbias,
                         cudaStream_t s) {
   using Sm = MainSmem<W, typename Io::T, kSlotBufs, NS>;
-  auto kern = bwd_main_kernel<Io, kVec, W, kMinBlocks, kSlotBufs, NS>;
+  auto kern = bwd_main_kernel<Io, kVec, W, kMinBlocks, kSlotBufs, NS, kKeepB>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sm::total);
   if (e != cudaSuccess) return e;
@@ -805,11 +814,17 @@ cudaError_t launch_bwd_t(int phase, const ScanArgs& a, const BwdOut& o, void* ws
     return cudaGetLastError();
   }
   if (phase == 1) {
-    // 4 warps per CTA, registers capped for three CTAs per SM (167 used, no
-    // spills), one dB/dC slot buffer so that three CTAs also fit in shared
-    // memory with 16 states: 12 warps per SM (measured fastest of 8/12
-    // warps, 1/2 buffers).  Larger state sizes fit fewer CTAs per SM.
-    return launch_main<Io, kVec, 4, 3, 1, NS>(a, o, w, sumS, sumQ, pBC, pA, pD, pbias, s);
+    // 16-bit I/O: 4 warps per CTA, registers capped for three CTAs per SM
+    // (168 used), one dB/dC slot buffer so that three CTAs also fit in
+    // shared memory with 16 states: 12 warps per SM (measured fastest of
+    // 8/12 warps, 1/2 buffers).  fp32 I/O: two CTAs per SM with B kept in
+    // registers and two slot buffers (one barrier fewer per state pair),
+    // measured 6% faster there and 10% slower for bf16.  Larger state
+    // sizes fit fewer CTAs per SM.
+    if constexpr (std::is_same<Io, IoF32>::value && NS <= 32)  // 64 states: no room for two buffers
+      return launch_main<Io, kVec, 4, 2, 2, NS, true>(a, o, w, sumS, sumQ, pBC, pA, pD, pbias, s);
+    else
+      return launch_main<Io, kVec, 4, 3, 1, NS, false>(a, o, w, sumS, sumQ, pBC, pA, pD, pbias, s);
   }
   const int64_t n = 2 * a.Bsz * NS * a.L;
   bwd_reduce_bc_kernel<NS><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(pBC, w.blocks, a.Bsz,
