@@ -17,6 +17,14 @@ inputs/outputs and float32 state and accumulation; synthetic seeded data
 Prints one JSON line on rank 0.  ``--impl reference`` times the fp64 CPU
 oracle (the method as plain sequential code) on a bounded sample of the same
 workload on this machine's host cores.
+
+Besides the step, rank 0 adds side measurements to the line (each with its
+roofline): the decode step at Bsz=256, Dch=5120; conv1d + silu forward and
+backward; the tensor-core input projection (x_proj + dt_proj); the fp32
+Mamba-370M layer forward + backward; the long-sequence forward
+(1 x 5120 x 131072); the bench layer with 64 states; and a four-piece chunked
+prefill continued from the carried state.  ``--profile-workload`` runs only
+one workload's kernels, for an ncu capture.
 """
 from __future__ import annotations
 
