@@ -21,7 +21,9 @@
  *
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The
- *     library allocates no memory and keeps no state between calls.
+ *     library allocates no memory.  The only state it keeps between calls
+ *     is the static scratch of ss_scan_bwd_noalloc and the failure counter
+ *     of ss_xproj_wait_failures.
  *   - Layouts are row-major with time innermost (no strides):
  *       u, delta, z, y, du, ddelta, dz, dy : [Bsz][Dch][L]   (I/O dtype)
  *       B, C                               : [Bsz][N][L]     (I/O dtype)
@@ -31,9 +33,10 @@
  *       h, h_last                          : [Bsz][Dch][N]   float32
  *     The I/O dtype (ss_dtype) is float32, bf16 or fp16 (16-bit patterns);
  *     arithmetic is float32 throughout, the state h is always float32.
- *   - Every pointer must be 16-byte aligned (SS_ERR_ALIGN otherwise).  Any
- *     L >= 0 is accepted; rows whose byte length is a multiple of 16 take the
- *     vectorised path, other L a slower element-wise path.
+ *   - Every pointer must be 16-byte aligned (SS_ERR_ALIGN otherwise).  The
+ *     scan, step and conv1d entry points accept any L >= 0: rows whose byte
+ *     length is a multiple of 16 take the vectorised path, other L a slower
+ *     element-wise path.  ss_xproj has its own shape rules (see its entry).
  *   - Optional inputs: D == NULL means D = 0, z == NULL means no gate,
  *     delta_bias == NULL means a zero bias.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
@@ -42,8 +45,9 @@
  *     a launch error (cudaGetLastError after the launch); faults during
  *     execution surface at the caller's next synchronisation.
  *   - Outputs are overwritten, never accumulated into.
- *   - N (the state size, d_state) is 8, 16, 32 or 64 (SS_ERR_N_UNSUPPORTED
- *     otherwise).  N = 16 is the tuned configuration.
+ *   - N (the state size, d_state) is 8, 16, 32 or 64 for the scan and step
+ *     entry points (SS_ERR_N_UNSUPPORTED otherwise).  N = 16 is the tuned
+ *     configuration.
  *   - Bsz is at most 65535 for the scan and step entry points (SS_ERR_SHAPE
  *     otherwise): the batch index is a grid dimension.
  */
