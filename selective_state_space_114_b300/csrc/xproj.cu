@@ -13,10 +13,11 @@
 // One CTA (8 warps) per tile of 128 tokens of one batch; one elected thread
 // issues tcgen05.mma (kind::f16, fp32 accumulators in tensor memory):
 //   GEMM 1  M = 128 tokens, N = R + 2N (padded to 16), K = Dch in chunks of
-//           64 channels.  A = u^T: the chunk [64 channels][128 tokens] is
+//           128 channels.  A = u^T: the chunk [128 channels][128 tokens] is
 //           copied by cp.async, then transposed into the K-major core-matrix
 //           layout with ldmatrix.trans; B = Wx, K-major as stored.  A ring
-//           of up to four stages keeps the copies of the next chunks in
+//           of stages (two with dt_rank 48 and 16 states; one when the
+//           weight tile is large) keeps the copy of the next chunk in
 //           flight while the MMAs of the current one run.
 //   epilogue 1  tcgen05.ld: B and C columns to global memory; the R dt
 //           columns rounded to the I/O type into shared memory (GEMM 2's A).
@@ -42,7 +43,7 @@ namespace {
 
 constexpr int kXpThreads = 256;  // 8 warps: two per tensor-memory lane quarter
 constexpr int kTokTile = 128;          // tokens per CTA (MMA M)
-constexpr int kKc = 64;                // channels per GEMM-1 chunk
+constexpr int kKc = 128;               // channels per GEMM-1 chunk (64: 10% slower)
 constexpr int kN2 = 128;               // delta channels per GEMM-2 step (MMA N)
 constexpr int kStageRowB = 2 * kTokTile + 16;  // u staging row bytes (padded)
 constexpr uint32_t kTmemCols = 512;
@@ -227,7 +228,7 @@ __global__ void __launch_bounds__(kXpThreads, 1) xproj_kernel(XprojArgs p) {
   auto aop_of = [&](int st) { return stage_of(st) + (size_t)kKc * kStageRowB; };
   auto bop_of = [&](int st) { return aop_of(st) + (size_t)kTokTile * kKc * 2; };
 
-  // cp.async of GEMM-1 chunk kc (channels kc*64 ..) into stage st
+  // cp.async of GEMM-1 chunk kc (channels kc * kKc ..) into stage st
   auto issue_chunk = [&](int kc, int st) {
     const int64_t k0 = (int64_t)kc * kKc;
     unsigned char* sg = stage_of(st);
@@ -274,15 +275,15 @@ __global__ void __launch_bounds__(kXpThreads, 1) xproj_kernel(XprojArgs p) {
     else
       cp_async_wait_all();
     failed = __syncthreads_or(failed);  // chunk kc staged by every thread
-    // transpose u [64 channels][128 tokens] into A core matrices (row = token)
+    // transpose u [kKc channels][128 tokens] into A core matrices (row = token)
     {
       const uint32_t sg = smem_u32(stage_of(st));
       unsigned char* ao = aop_of(st);
-      // 128 core matrices (16 token groups x 8 channel groups), 16 per warp,
-      // four per ldmatrix: matrix m of the instruction = token group rg0 + m
+      // 16 token groups x kKc / 8 channel groups of core matrices, four per
+      // ldmatrix (matrix m of the instruction = token group rg0 + m)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int idx = warp * 4 + q;  // 0..31: (kg, rg0 / 4)
+      for (int q = 0; q < kKc / 16; ++q) {
+        const int idx = warp * (kKc / 16) + q;  // (kg, rg0 / 4)
         const int kg = idx >> 2, rg0 = (idx & 3) * 4;
         const int m = lane >> 3, i = lane & 7;
         uint32_t r[4];
