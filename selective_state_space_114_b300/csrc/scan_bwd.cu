@@ -85,8 +85,10 @@ __device__ __forceinline__ float step_delta(float raw, float bias, int softplus)
 // ---------------------------------------------------------------------------
 // NS states in groups of SG = min(NS, 16): grid z = NS / SG, each thread
 // holds the SG states of its group (states SG z .. SG z + SG - 1).
+// Registers capped for four CTAs per SM (128): 5% faster than three with
+// bf16 I/O, the same with fp32.
 template <typename Io, bool kVec, int NS>
-__global__ void __launch_bounds__(kSumThreads)
+__global__ void __launch_bounds__(kSumThreads, 4)
     bwd_summary_kernel(ScanArgs p, BwdOut o, int64_t nrb, float* __restrict__ sumS,
                        float* __restrict__ sumQ, float* __restrict__ dsum_out) {
   using T = typename Io::T;
