@@ -52,7 +52,7 @@ def inputs_to_dev(x: dict, dtype: str) -> dict:
         if v is None:
             out[k] = None
         elif k in ("A", "D", "delta_bias"):
-            out[k] = torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).cuda()
+            out[k] = torch.from_numpy(np.array(v, dtype=np.float32)).cuda()
         else:
             out[k] = to_dev(v, dtype)
     return out
