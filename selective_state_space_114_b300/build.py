@@ -20,6 +20,9 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 SO = os.path.join(HERE, "libselscan.so")
+# pipe-rate microbenchmark the bench uses for its ALU roofline denominators
+PROBE_SRC = os.path.join(HERE, "probe", "pipes.cu")
+PROBE_SO = os.path.join(HERE, "libssprobe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -46,7 +49,22 @@ def stale() -> bool:
     return any(os.path.getmtime(p) > t for p in deps())
 
 
+def build_probe(force: bool = False) -> str:
+    if not force and os.path.exists(PROBE_SO) and \
+            os.path.getmtime(PROBE_SO) >= os.path.getmtime(PROBE_SRC):
+        return PROBE_SO
+    tmp = PROBE_SO + f".tmp{os.getpid()}"
+    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "--shared", "-Xcompiler", "-fPIC",
+           "--cudart", "shared", "-o", tmp, PROBE_SRC]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("nvcc failed:\n" + r.stdout + r.stderr)
+    os.replace(tmp, PROBE_SO)
+    return PROBE_SO
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
+    build_probe(force)
     if not force and not stale():
         return SO
     tmp = SO + f".tmp{os.getpid()}"
