@@ -77,12 +77,26 @@ typedef enum {
     SS_ERR_ALIGN = 5,          /* a pointer is not 16-byte aligned                */
     SS_ERR_WORKSPACE = 6,      /* workspace NULL/misaligned or smaller than needed */
     SS_ERR_CUDA = 7,           /* the CUDA runtime reported a launch error        */
-    SS_ERR_SCRATCH_LIMIT = 8   /* ss_scan_bwd_noalloc: problem needs more scratch
+    SS_ERR_SCRATCH_LIMIT = 8,  /* ss_scan_bwd_noalloc: problem needs more scratch
                                   than the library's static buffer holds          */
+    SS_ERR_TIMEOUT = 9         /* a kernel's bounded wait on the hardware gave up
+                                  (reported by ss_check_device_errors)            */
 } ss_status;
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* ss_status_str(ss_status s);
+
+/*
+ * Device-side failures since the last check.  Kernels that wait on hardware
+ * (ss_xproj waits on tensor-core completion barriers) bound every wait; a
+ * wait that gives up sets a bit in a device error word, skips the rest of
+ * its work (the outputs of that call are incomplete) and lets the kernel
+ * finish.  This call synchronises stream, reads the word of the current
+ * device, clears it and returns SS_ERR_TIMEOUT if any bit was set, SS_OK if
+ * none, SS_ERR_CUDA if the copy itself failed.  The word is per device and
+ * shared by all streams.
+ */
+ss_status ss_check_device_errors(ss_stream_t stream);
 
 /* Library ABI version: major * 10000 + minor * 100 + patch. */
 int ss_version(void);
@@ -129,10 +143,15 @@ ss_status ss_scan_bwd_workspace_size(int64_t Bsz, int64_t Dch, int64_t L, int64_
 
 /*
  * Backward of ss_scan_fwd (zero initial state) for an upstream gradient dy
- * of y.  The state trajectory is recomputed, not stored: the workspace holds
- * the states at 16-step segment boundaries and per-block partial sums of
- * dA, dB, dC, dD and ddelta_bias, reduced in a fixed order, so reruns are
- * bitwise identical.
+ * of y.  As the "mamba.py" page (gittoolsai.com, section 性能, performance)
+ * describes for the hardware-aware scan, the backward recomputes the forward's
+ * intermediate states instead of storing them; the adjoint recurrence runs in
+ * reverse time (the same page's TODO list: the scan on time-flipped arrays).
+ * The sequence is cut into 128-step chunks: the workspace holds, per (row,
+ * chunk), the state entering the chunk and the adjoint carry entering it
+ * from the later chunk (from a summary pass over every chunk), plus
+ * per-block partial sums of dA, dB, dC, dD and ddelta_bias, reduced in a
+ * fixed order, so reruns are bitwise identical.
  *   in : the forward's inputs, dy [Bsz][Dch][L] (I/O dtype),
  *        workspace (device, 16-byte aligned, >= ss_scan_bwd_workspace_size).
  *   out: du, ddelta (gradient of delta_raw), dz [Bsz][Dch][L] in the I/O
@@ -154,8 +173,9 @@ ss_status ss_scan_bwd(const void* u, const void* delta, const float* A, const vo
  * exactly ss_scan_bwd's arguments and performs the same checks; calling the
  * three in order on one stream (same arguments, same workspace) is
  * ss_scan_bwd.
- *   ss_scan_bwd_states : recomputes the forward states at every 16-step
- *                        segment boundary into the workspace.
+ *   ss_scan_bwd_states : the chunk summaries and carries: the state and the
+ *                        adjoint carry entering every 128-step chunk, into
+ *                        the workspace.
  *   ss_scan_bwd_reverse: the reverse-time pass; writes du, ddelta, dz and
  *                        the per-block partial sums of dA, dB, dC, dD,
  *                        ddelta_bias into the workspace.
@@ -253,10 +273,21 @@ ss_status ss_xproj(const void* u, const void* Wx, const void* Wdt, int64_t Bsz, 
 
 /*
  * Number of ss_xproj CTAs (since the library was loaded) whose bounded wait
- * for the tensor cores gave up; such a CTA leaves its outputs incomplete.
+ * for the tensor cores gave up; such a CTA leaves its outputs incomplete and
+ * also sets the device error word that ss_check_device_errors reports.
  * Synchronous (device-to-host copy on the legacy stream); -1 on a CUDA error.
  */
 int ss_xproj_wait_failures(void);
+
+/*
+ * Test hook for the timeout path: while on != 0, every ss_xproj CTA, after
+ * its first GEMM, also waits (for 64 polls) on a barrier that nothing ever
+ * completes, so that wait gives up and the CTA takes its failure path (the
+ * tensor-core work already issued completes and is waited for; the outputs
+ * are left unwritten).  Lets a test check that SS_ERR_TIMEOUT is reported
+ * without faulting or hanging the device.  Off by default.
+ */
+void ss_debug_xproj_stuck_wait(int on);
 
 /*
  * Backward scan for callers that cannot allocate device memory.
@@ -271,12 +302,15 @@ int ss_xproj_wait_failures(void);
  * ss_scan_bwd_noalloc_max_scratch() bytes (32 MiB), which every GPU that
  * loads the library holds until the process exits.
  *   - Arguments, checks, outputs and results are those of ss_scan_bwd,
- *     without the workspace pair.
- *   - Sizes whose ss_scan_bwd_workspace_size exceeds the buffer are
+ *     without the workspace pair; its argument checks run first.
+ *   - Then sizes whose ss_scan_bwd_workspace_size exceeds the buffer are
  *     rejected with SS_ERR_SCRATCH_LIMIT; nothing is launched.
  *   - The first call on a device looks up the buffer's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture starts.
+ *     (cudaGetSymbolAddress, with that device current) and caches it.  With
+ *     lazy module loading (the CUDA default) this lookup is what loads the
+ *     library's device code and the buffer onto that device, so the first
+ *     call does take device memory: make it at initialisation, outside
+ *     allocation-sensitive code and before any stream capture starts.
  *   - The call allocates nothing (no cudaMalloc, cudaFree or allocating
  *     library routine).
  *   - All calls share the one buffer, which keeps the last call's contents;

@@ -32,6 +32,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libselscan.so")
 
 SS_F32, SS_BF16, SS_F16 = 0, 1, 2
+SS_OK, SS_ERR_TIMEOUT = 0, 9
 N_STATE = 16
 
 
@@ -73,6 +74,10 @@ def _load() -> ctypes.CDLL:
     lib.ss_xproj.restype = ci
     lib.ss_xproj_wait_failures.argtypes = []
     lib.ss_xproj_wait_failures.restype = ci
+    lib.ss_check_device_errors.argtypes = [p]
+    lib.ss_check_device_errors.restype = ci
+    lib.ss_debug_xproj_stuck_wait.argtypes = [ci]
+    lib.ss_debug_xproj_stuck_wait.restype = None
     lib.ss_conv1d_silu_fwd.argtypes = [p, p, p, ci, i64, i64, i64, i64, ci, p, p]
     lib.ss_conv1d_silu_fwd.restype = ci
     lib.ss_conv1d_silu_bwd.argtypes = [p, p, p, ci, p, i64, i64, i64, i64, ci, p, p, p, p]
@@ -90,7 +95,8 @@ EXPORTED_SYMBOLS = ("ss_status_str", "ss_version", "ss_scan_fwd", "ss_scan_fwd_f
                     "ss_scan_bwd", "ss_scan_bwd_states", "ss_scan_bwd_reverse",
                     "ss_scan_bwd_reduce", "ss_step", "ss_conv1d_silu_fwd",
                     "ss_conv1d_silu_bwd", "ss_scan_bwd_noalloc",
-                    "ss_scan_bwd_noalloc_max_scratch", "ss_xproj", "ss_xproj_wait_failures")
+                    "ss_scan_bwd_noalloc_max_scratch", "ss_xproj", "ss_xproj_wait_failures",
+                    "ss_check_device_errors", "ss_debug_xproj_stuck_wait")
 
 
 def lib() -> ctypes.CDLL:
@@ -329,3 +335,15 @@ def ss_xproj(u, Wx, Wdt, N, out=None):
 
 def ss_xproj_wait_failures() -> int:
     return int(_lib.ss_xproj_wait_failures())
+
+
+def ss_check_device_errors(device=None) -> int:
+    """Status of the device error word since the last check (SS_OK or
+    SS_ERR_TIMEOUT); synchronises the current stream and clears the word."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    return int(_lib.ss_check_device_errors(_stream(dev)))
+
+
+def ss_debug_xproj_stuck_wait(on: bool) -> None:
+    """Test hook: make every later ss_xproj CTA give up one bounded wait."""
+    _lib.ss_debug_xproj_stuck_wait(1 if on else 0)

@@ -50,6 +50,9 @@ const char* ss_status_str(ss_status s) {
     case SS_ERR_SCRATCH_LIMIT:
       return "SS_ERR_SCRATCH_LIMIT: the problem needs more scratch than the static buffer of "
              "ss_scan_bwd_noalloc holds";
+    case SS_ERR_TIMEOUT:
+      return "SS_ERR_TIMEOUT: a kernel's bounded wait on the hardware gave up (its outputs are "
+             "incomplete)";
   }
   return "unknown ss_status";
 }
@@ -127,7 +130,7 @@ ss_status check_bwd(const void* u, const void* delta, const float* A, const void
                     const void* dy, int64_t Bsz, int64_t Dch, int64_t L, int64_t N,
                     ss_dtype dtype, void* du, void* ddelta, float* dA, float* dB, float* dC,
                     float* dD, void* dz, float* ddelta_bias, void* workspace,
-                    size_t workspace_bytes, bool* work) {
+                    size_t workspace_bytes, bool* work, bool check_workspace = true) {
   if (!known_dtype(dtype)) return SS_ERR_DTYPE;
   if (bad_size(Bsz) || bad_size(Dch) || bad_size(L) || bad_size(N)) return SS_ERR_SHAPE;
   if (Bsz > 65535 || product_too_big(Bsz, Dch, L)) return SS_ERR_SHAPE;
@@ -143,7 +146,7 @@ ss_status check_bwd(const void* u, const void* delta, const float* A, const void
       misaligned(du) || misaligned(ddelta) || misaligned(dA) || misaligned(dB) ||
       misaligned(dC) || misaligned(dD) || misaligned(dz) || misaligned(ddelta_bias))
     return SS_ERR_ALIGN;
-  if (*work) {
+  if (*work && check_workspace) {
     const size_t need = selscan::bwd_workspace_bytes(Bsz, Dch, L, N);
     if (!workspace || misaligned(workspace) || workspace_bytes < need) return SS_ERR_WORKSPACE;
   }
@@ -196,6 +199,18 @@ ss_status run_bwd(int phase, const void* u, const void* delta, const float* A, c
 }
 
 }  // namespace
+
+// ss_scan_bwd's argument checks without the workspace pair (for
+// ss_scan_bwd_noalloc, which supplies its own); internal to the library.
+__attribute__((visibility("hidden"))) ss_status selscan_check_bwd_args(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, const void* dy, int64_t Bsz,
+    int64_t Dch, int64_t L, int64_t N, ss_dtype dtype, void* du, void* ddelta, float* dA,
+    float* dB, float* dC, float* dD, void* dz, float* ddelta_bias) {
+  bool work = false;
+  return check_bwd(u, delta, A, B, C, D, z, delta_bias, dy, Bsz, Dch, L, N, dtype, du, ddelta,
+                   dA, dB, dC, dD, dz, ddelta_bias, nullptr, 0, &work, false);
+}
 
 #define SS_BWD_PARAMS                                                                        \
   const void *u, const void *delta, const float *A, const void *B, const void *C,             \
@@ -272,6 +287,20 @@ ss_status ss_conv1d_silu_bwd(const void* x, const float* w, const float* bias, i
   return cuda_status(selscan::launch_conv(1, a, o, s));
 }
 
+namespace {
+int g_xproj_stuck_wait = 0;  // test hook state (ss_debug_xproj_stuck_wait)
+}  // namespace
+
+ss_status ss_check_device_errors(ss_stream_t stream) {
+  unsigned int flags = 0;
+  if (selscan::read_clear_error_flags(reinterpret_cast<cudaStream_t>(stream), &flags) !=
+      cudaSuccess)
+    return SS_ERR_CUDA;
+  return flags ? SS_ERR_TIMEOUT : SS_OK;
+}
+
+void ss_debug_xproj_stuck_wait(int on) { g_xproj_stuck_wait = on ? 1 : 0; }
+
 ss_status ss_xproj(const void* u, const void* Wx, const void* Wdt, int64_t Bsz, int64_t Dch,
                    int64_t L, int64_t R, int64_t N, ss_dtype dtype, void* delta, void* B, void* C,
                    ss_stream_t stream) {
@@ -287,7 +316,10 @@ ss_status ss_xproj(const void* u, const void* Wx, const void* Wdt, int64_t Bsz, 
       misaligned(C))
     return SS_ERR_ALIGN;
   if (!work) return SS_OK;
-  selscan::XprojArgs a{u, Wx, Wdt, Bsz, Dch, L, R, N, to_dt(dtype), delta, B, C};
+  unsigned int* err = nullptr;
+  if (selscan::error_flags_ptr(&err) != cudaSuccess) return SS_ERR_CUDA;
+  selscan::XprojArgs a{u, Wx, Wdt, Bsz, Dch, L, R, N, to_dt(dtype), delta, B, C, err,
+                       g_xproj_stuck_wait};
   return cuda_status(selscan::launch_xproj(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

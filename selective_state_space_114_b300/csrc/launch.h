@@ -64,6 +64,13 @@ size_t bwd_workspace_bytes(int64_t Bsz, int64_t Dch, int64_t L, int64_t N);
 cudaError_t launch_scan_bwd(int phase, const ScanArgs& a, const BwdOut& o, void* ws,
                             cudaStream_t s);
 
+// The library's device error word: bits set by kernels whose bounded waits
+// gave up.  error_flags_ptr: its device address on the current device;
+// read_clear_error_flags: copy it to the host and clear it (synchronises s).
+constexpr unsigned int kErrXprojTimeout = 1u << 0;  // input projection: a tensor-core wait
+cudaError_t error_flags_ptr(unsigned int** out);
+cudaError_t read_clear_error_flags(cudaStream_t s, unsigned int* out);
+
 // One decode step.  Requires Bsz*Dch > 0.
 cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
 
@@ -98,6 +105,8 @@ struct XprojArgs {
   void* delta;      // [Bsz][Dch][L]
   void* B;          // [Bsz][N][L]
   void* C;          // [Bsz][N][L]
+  unsigned int* err = nullptr;     // device error word (kErrXprojTimeout)
+  int test_stuck_wait = 0;         // test hook: also wait on a barrier nothing arrives at
 };
 
 // Input projection (x_proj then dt_proj) on the tensor cores.  Requires

@@ -17,7 +17,11 @@
 // In host code the array's name does not denote a device address, so the
 // first call on each device looks the address up with cudaGetSymbolAddress
 // (with that device current) and caches it; later calls reuse the cached
-// address.  Make that first call before any stream capture begins.
+// address.  With lazy module loading (the CUDA default) that first lookup is
+// also what loads the library's device code, and with it the array, onto the
+// device: the first call on a device does take device memory.  Make it at
+// initialisation, outside allocation-sensitive code and before any stream
+// capture begins.
 //
 // All calls share the one buffer and it keeps whatever the last call left
 // in it.  The backward kernels write every scratch word before they read
@@ -30,6 +34,13 @@
 #include <mutex>
 
 #include "../../include/selscan.h"
+
+// ss_scan_bwd's argument checks (api.cu), without the workspace pair.
+extern "C" ss_status selscan_check_bwd_args(
+    const void* u, const void* delta, const float* A, const void* B, const void* C,
+    const float* D, const void* z, const float* delta_bias, const void* dy, int64_t Bsz,
+    int64_t Dch, int64_t L, int64_t N, ss_dtype dtype, void* du, void* ddelta, float* dA,
+    float* dB, float* dC, float* dD, void* dz, float* ddelta_bias);
 
 constexpr size_t kScratchBytes = size_t(32) << 20;  // 32 MiB
 
@@ -68,8 +79,13 @@ ss_status ss_scan_bwd_noalloc(const void* u, const void* delta, const float* A, 
                               int64_t Bsz, int64_t Dch, int64_t L, int64_t N, ss_dtype dtype,
                               void* du, void* ddelta, float* dA, float* dB, float* dC,
                               float* dD, void* dz, float* ddelta_bias, ss_stream_t stream) {
+  // ss_scan_bwd's checks first (same status for the same bad arguments),
+  // then the scratch limit
+  ss_status st = selscan_check_bwd_args(u, delta, A, B, C, D, z, delta_bias, dy, Bsz, Dch, L, N,
+                                         dtype, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias);
+  if (st != SS_OK) return st;
   size_t need = 0;
-  ss_status st = ss_scan_bwd_workspace_size(Bsz, Dch, L, N, dtype, &need);
+  st = ss_scan_bwd_workspace_size(Bsz, Dch, L, N, dtype, &need);
   if (st != SS_OK) return st;
   if (need > kScratchBytes) return SS_ERR_SCRATCH_LIMIT;
   void* ws = nullptr;

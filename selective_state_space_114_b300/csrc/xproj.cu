@@ -60,10 +60,11 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 }
 
 // Wait for the completion of the mbarrier phase with the given parity;
-// false after kWaitIters polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// false after `polls` polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint32_t polls = kWaitIters) {
   const uint32_t a = smem_u32(bar);
-  for (uint32_t i = 0; i < kWaitIters; ++i) {
+  for (uint32_t i = 0; i < polls; ++i) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -188,7 +189,7 @@ __global__ void __launch_bounds__(kXpThreads, 1) xproj_kernel(XprojArgs p) {
   using T = typename Io::T;
   constexpr bool kBf16 = std::is_same<Io, IoBf16>::value;
   extern __shared__ __align__(1024) unsigned char xsm[];
-  __shared__ uint64_t bar1, bar2[2];
+  __shared__ uint64_t bar1, bar2[2], bar_never;
   __shared__ uint32_t tmem_slot;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -214,6 +215,7 @@ __global__ void __launch_bounds__(kXpThreads, 1) xproj_kernel(XprojArgs p) {
     mbar_init(&bar1, 1);
     mbar_init(&bar2[0], 1);
     mbar_init(&bar2[1], 1);
+    mbar_init(&bar_never, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   tc_fence_before();
@@ -313,6 +315,9 @@ __global__ void __launch_bounds__(kXpThreads, 1) xproj_kernel(XprojArgs p) {
   }
   if (!failed && !mbar_wait(&bar1, ph1 & 1)) failed = true;
   ++ph1;
+  // test hook: a wait on a barrier nothing arrives at, which must give up
+  // (the MMAs issued so far complete normally; the drain below waits for them)
+  if (p.test_stuck_wait && !failed && !mbar_wait(&bar_never, 0, 64)) failed = true;
   cp_async_wait_all();  // the trailing empty groups
   failed = __syncthreads_or(failed);
   tc_fence_after();
@@ -431,6 +436,7 @@ __global__ void __launch_bounds__(kXpThreads, 1) xproj_kernel(XprojArgs p) {
   if (failed) {
     if (tid == 0) {
       atomicAdd(&g_xproj_wait_failures, 1);
+      if (p.err) atomicOr(p.err, kErrXprojTimeout);
       // the CTA's MMAs may still be in flight: wait (bounded) for the last
       // commit on each barrier
       if (c1) mbar_wait(&bar1, (c1 - 1) & 1);

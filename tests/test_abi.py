@@ -32,9 +32,10 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_status_strings():
-    for code in range(8):
+    for code in range(10):
         s = ss.ss_status_str(code)
         assert s and s.startswith("SS_")
+    assert ss.ss_status_str(ss.SS_ERR_TIMEOUT).startswith("SS_ERR_TIMEOUT")
     assert ss.ss_status_str(99) == "unknown ss_status"
     assert ss.ss_version() >= 10000
 
@@ -224,3 +225,38 @@ def test_xproj_rejects(kw, code):
 
 def test_xproj_empty_is_ok_without_pointers():
     assert xproj(u=None, Wx=None, Wdt=None, delta=None, B=None, C=None, L=0) == OK
+
+
+def noalloc(**kw):
+    a = dict(u=P, delta=P, A=P, B=P, C=P, D=P, z=P, bias=P, softplus=1, dy=P, Bsz=2, Dch=16,
+             L=64, N=16, dtype=1, du=P, dd=P, dA=P, dB=P, dC=P, dD=P, dz=P, dbias=P)
+    a.update(kw)
+    return ss.lib().ss_scan_bwd_noalloc(
+        a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["bias"], a["softplus"],
+        a["dy"], a["Bsz"], a["Dch"], a["L"], a["N"], a["dtype"], a["du"], a["dd"], a["dA"],
+        a["dB"], a["dC"], a["dD"], a["dz"], a["dbias"], None)
+
+
+BIG = dict(Bsz=4, Dch=1024, L=4096)  # needs more than the 32 MiB static buffer
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=5), DTYPE),
+    (dict(N=4), NUNS),
+    (dict(dy=None), NULL),
+    (dict(dD=None), NULL),
+    (dict(du=MIS), ALIGN),
+    # ss_scan_bwd's argument checks come before the scratch limit
+    (dict(dy=None, **BIG), NULL),
+    (dict(du=MIS, **BIG), ALIGN),
+    (dict(BIG), 8),                 # SS_ERR_SCRATCH_LIMIT
+])
+def test_noalloc_rejects_like_ss_scan_bwd_then_by_size(kw, code):
+    assert noalloc(**kw) == code
+
+
+def test_check_device_errors_without_a_device_reports_a_cuda_error():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("covered by the GPU tests")
+    assert ss.lib().ss_check_device_errors(None) == 7  # SS_ERR_CUDA

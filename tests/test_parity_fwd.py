@@ -24,7 +24,7 @@ def compare(x, dtype, softplus=True, what=""):
     torch.cuda.synchronize()
     ref, href = oracle_fwd(x, softplus)
     check(to_host64(y), ref, out_kind(dtype), f"{what} y")
-    check(to_host64(hl), href, "f32" if dtype == "f32" else "bf16", f"{what} h_last")
+    check(to_host64(hl), href, "f32", f"{what} h_last")
 
 
 def test_tiny_config_f32():
@@ -108,49 +108,65 @@ def test_deterministic():
     assert torch.equal(y1, y2) and torch.equal(h1, h2)
 
 
-def _row_oracle(cfg, b, d):
-    r = synth.row_inputs(cfg, b, d)
-    w = widen_all(r)
+def _rows_oracle(cfg, rows):
+    """fp64 oracle on the (b, d) rows of a workload, regenerated on their own
+    (one oracle call per batch over the sampled channels, all host cores)."""
     L, N = cfg["L"], cfg["N"]
-    out, hl = oracle.scan_fwd(w["u"].reshape(1, 1, L), w["delta"].reshape(1, 1, L),
-                              w["A"].reshape(1, N), w["B"].reshape(1, N, L),
-                              w["C"].reshape(1, N, L), w["D"], w["z"].reshape(1, 1, L),
-                              w["delta_bias"], True)
-    return out[0, 0], hl[0, 0]
+    out = {}
+    for b in sorted({b for b, _ in rows}):
+        ds = [d for bb, d in rows if bb == b]
+        rs = [widen_all(synth.row_inputs(cfg, b, d)) for d in ds]
+        st = lambda k: np.stack([r[k] for r in rs]).reshape(1, len(ds), L)
+        y, hl = oracle.scan_fwd(st("u"), st("delta"), np.stack([r["A"] for r in rs]),
+                                rs[0]["B"].reshape(1, N, L), rs[0]["C"].reshape(1, N, L),
+                                np.concatenate([r["D"] for r in rs]), st("z"),
+                                np.concatenate([r["delta_bias"] for r in rs]), True)
+        for i, d in enumerate(ds):
+            out[(b, d)] = (y[0, i], hl[0, i])
+    return out
 
 
-def _full_config_sampled(index, rows):
-    cfg = synth.config(index)
+def _check_long_rows(got, ref):
+    """The error, relative to the bound, must not grow along the sequence."""
+    L = got.shape[-1]
+    err = np.abs(got - ref) / (2e-2 * (np.abs(ref) + 1e-2))
+    per = err[: (L // 4096) * 4096].reshape(-1, 4096).max(axis=1)
+    assert per.max() <= 1.0
+
+
+def test_config1_full_size_every_element():
+    """The bf16 Mamba-130M layer (8 x 1536 x 2048): every output and final
+    state against the fp64 oracle over the whole workload."""
+    cfg = synth.config(1)
+    x = synth.make_inputs(cfg)
+    xd = inputs_to_dev(x, cfg["dtype"])
+    y, hl = run_fwd(xd)
+    torch.cuda.synchronize()
+    ref, href = oracle_fwd(x)
+    check(to_host64(y), ref, "bf16", "config 1 y")
+    check(to_host64(hl), href, "f32", "config 1 h_last")
+
+
+def test_config3_full_size_sampled_rows():
+    """1 x 5120 x 131072 bf16 (too large for a whole-workload oracle pass):
+    64 sampled rows, including both ends, every step of each."""
+    cfg = synth.config(3)
     x = synth.make_inputs(cfg)
     xd = inputs_to_dev(x, cfg["dtype"])
     del x
     y, hl = run_fwd(xd)
     torch.cuda.synchronize()
     assert torch.isfinite(y.float()).all()
-    L = cfg["L"]
-    for b, d in rows:
-        ref, href = _row_oracle(cfg, b, d)
-        got = to_host64(y[b, d])
-        check(got, ref, out_kind(cfg["dtype"]), f"config {index} row ({b},{d})")
-        check(to_host64(hl[b, d]), href, "bf16", f"config {index} h_last ({b},{d})")
-        # error per chunk of L, relative to the bound, must not grow along the sequence
-        if L >= 8192:
-            err = np.abs(got - ref) / (2e-2 * (np.abs(ref) + 1e-2))
-            per = err[: (L // 4096) * 4096].reshape(-1, 4096).max(axis=1)
-            assert per.max() <= 1.0
-
-
-def test_config1_full_size_sampled_rows():
-    rng = np.random.default_rng(1)
-    rows = [(0, 0), (7, 1535), (3, 767)] + [(int(rng.integers(8)), int(rng.integers(1536)))
-                                            for _ in range(29)]
-    _full_config_sampled(1, rows)
-
-
-def test_config3_full_size_sampled_rows():
     rng = np.random.default_rng(3)
-    rows = [(0, 0), (0, 5119)] + [(0, int(rng.integers(5120))) for _ in range(6)]
-    _full_config_sampled(3, rows)
+    ds = sorted({0, 5119, *[int(v) for v in rng.choice(5120, size=62, replace=False)]})
+    rows = [(0, d) for d in ds]
+    refs = _rows_oracle(cfg, rows)
+    for b, d in rows:
+        ref, href = refs[(b, d)]
+        got = to_host64(y[b, d])
+        check(got, ref, "bf16", f"config 3 row ({b},{d})")
+        check(to_host64(hl[b, d]), href, "f32", f"config 3 h_last ({b},{d})")
+        _check_long_rows(got, ref)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
@@ -163,12 +179,17 @@ def test_softplus_extremes(dtype):
     compare(x, dtype, what=f"{dtype} softplus extremes")
 
 
-def test_config2_full_size_forward_sampled_rows():
-    """8 x 2048 x 2048 float32 forward (the fp32 kernel configuration) on sampled rows."""
-    rng = np.random.default_rng(2)
-    rows = [(0, 0), (7, 2047), (4, 1024)] + [(int(rng.integers(8)), int(rng.integers(2048)))
-                                            for _ in range(13)]
-    _full_config_sampled(2, rows)
+def test_config2_full_size_forward_every_element():
+    """8 x 2048 x 2048 float32 forward (the fp32 kernel configuration): every
+    output and final state against the fp64 oracle."""
+    cfg = synth.config(2)
+    x = synth.make_inputs(cfg)
+    xd = inputs_to_dev(x, "f32")
+    y, hl = run_fwd(xd)
+    torch.cuda.synchronize()
+    ref, href = oracle_fwd(x)
+    check(to_host64(y), ref, "f32", "config 2 y")
+    check(to_host64(hl), href, "f32", "config 2 h_last")
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
@@ -201,7 +222,7 @@ def test_from_state_matches_oracle(dtype, Bsz, Dch, L):
     torch.cuda.synchronize()
     ref, href = oracle_fwd(x, True, h0=h0.astype(np.float64))
     check(to_host64(y), ref, out_kind(dtype), f"{dtype} from state y")
-    check(to_host64(hl), href, "f32" if dtype == "f32" else out_kind(dtype), "from state h_last")
+    check(to_host64(hl), href, "f32", "from state h_last")
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -223,7 +244,7 @@ def test_two_chunks_in_place_equal_one_scan(dtype):
     assert h2.data_ptr() == h.data_ptr()
     ref, href = oracle_fwd(x, True)
     check(to_host64(torch.cat([y1, y2], dim=-1)), ref, out_kind(dtype), f"{dtype} chunked y")
-    check(to_host64(h), href, "f32" if dtype == "f32" else "bf16", "chunked final state")
+    check(to_host64(h), href, "f32", "chunked final state")
 
 
 def test_from_state_empty_sequence_copies_the_state():
@@ -283,7 +304,7 @@ def test_rows_kernel_from_state_in_place(dtype):
     assert hl.data_ptr() == h.data_ptr()
     ref, href = oracle_fwd(x, True, h0=h0.astype(np.float64))
     check(to_host64(y), ref, out_kind(dtype), f"rows {dtype} from state y")
-    check(to_host64(hl), href, "f32" if dtype == "f32" else out_kind(dtype), "rows h_last")
+    check(to_host64(hl), href, "f32", "rows h_last")
 
 
 def test_rows_kernel_deterministic():

@@ -19,7 +19,9 @@ NS = [8, 32, 64]
 
 
 def h_kind(dtype):
-    return "f32" if dtype == "f32" else out_kind(dtype)
+    # the state is float32 whatever the I/O type; the oracle runs on the same
+    # rounded inputs, so h takes the fp32 bar
+    return "f32"
 
 
 @pytest.mark.parametrize("N", NS)
@@ -67,7 +69,7 @@ def test_forward_many_rows(N):
     torch.cuda.synchronize()
     ref, href = oracle_fwd(x)
     check(to_host64(y), ref, "bf16", f"N={N} many rows y")
-    check(to_host64(hl), href, "bf16", f"N={N} many rows h_last")
+    check(to_host64(hl), href, "f32", f"N={N} many rows h_last")
 
 
 @pytest.mark.parametrize("N", NS)
@@ -127,7 +129,7 @@ def test_scan_then_step_equals_longer_scan(N):
                         xd["delta_bias"], True)
         torch.cuda.synchronize()
         check(to_host64(yt), ref[..., t], "bf16", f"N={N} token {t}")
-    check(to_host64(h), href, "bf16", f"N={N} state after steps")
+    check(to_host64(h), href, "f32", f"N={N} state after steps")
 
 
 IO_GRADS = ("du", "ddelta", "dz")

@@ -73,7 +73,7 @@ def test_scan_then_step_equals_longer_scan(dtype):
                         xd["delta_bias"], True)
         torch.cuda.synchronize()
         check(to_host64(yt), ref[..., t], out_kind(dtype), f"token {t}")
-    check(to_host64(h), href, "f32" if dtype == "f32" else "bf16", "state after steps")
+    check(to_host64(h), href, "f32", "state after steps")
 
 
 def test_config4_128_steps_state_checked_every_step():

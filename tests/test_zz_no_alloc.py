@@ -3,10 +3,11 @@
 Some callers cannot call cudaMalloc (a plugin inside an application that
 owns all device memory, or a loop that must never enter the allocator).
 This entry point takes no workspace; it uses a static scratch buffer inside
-the library instead.  Its results must match ss_scan_bwd's within the
-gradient tolerance of the other backward tests, on consecutive calls that
-leave different contents in the shared buffer, and problems larger than the
-buffer must be refused before anything runs.
+the library instead.  It runs the same kernels as ss_scan_bwd, so its results
+must equal ss_scan_bwd's bit for bit, on consecutive calls that leave
+different contents in the shared buffer; the first call is also checked
+against the fp64 oracle.  Problems larger than the buffer must be refused
+before anything runs.
 
 Called through the C ABI (ctypes), not through a Python wrapper.
 """
@@ -15,7 +16,7 @@ import ctypes
 import pytest
 import torch
 
-from parity_util import check, grad_kind, inputs_to_dev, make_case, to_dev, to_host64
+from parity_util import check, grad_kind, inputs_to_dev, make_case, oracle_bwd, to_dev, to_host64
 
 import selective_state_space_114_b300 as ss
 
@@ -48,10 +49,11 @@ def _noalloc(xd, dyd, g):
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
-def _case(dtype, Bsz, Dch, L, seed):
+def _case(dtype, Bsz, Dch, L, seed, host=False):
     x = make_case(dtype, Bsz, Dch, L, seed=seed, with_dy=True)
     dy = x.pop("dy")
-    return inputs_to_dev(x, dtype), to_dev(dy, dtype)
+    dev = (inputs_to_dev(x, dtype), to_dev(dy, dtype))
+    return dev + (x, dy) if host else dev
 
 
 def test_noalloc_matches_workspace_backward_on_consecutive_calls():
@@ -59,17 +61,20 @@ def test_noalloc_matches_workspace_backward_on_consecutive_calls():
     assert limit == 32 << 20
     # the second call runs on a smaller problem, over the first call's leftovers
     cases = [("bf16", 3, 40, 1000, 41), ("f32", 2, 17, 300, 43)]
-    for dtype, Bsz, Dch, L, seed in cases:
+    for i, (dtype, Bsz, Dch, L, seed) in enumerate(cases):
         assert ss.ss_scan_bwd_workspace_size(Bsz, Dch, L) <= limit
-        xd, dyd = _case(dtype, Bsz, Dch, L, seed)
+        xd, dyd, x, dy = _case(dtype, Bsz, Dch, L, seed, host=True)
         g = _alloc_grads(xd)
         assert _noalloc(xd, dyd, g) == SS_OK
         ref = ss.ss_scan_bwd(xd["u"], xd["delta"], xd["A"], xd["B"], xd["C"], xd["D"], xd["z"],
                              xd["delta_bias"], True, dyd)
         torch.cuda.synchronize()
         for k in NAMES:
-            check(to_host64(g[k]), to_host64(ref[k]), grad_kind(dtype, k in IO),
-                  f"noalloc {dtype} {k}")
+            assert torch.equal(g[k], ref[k]), f"noalloc {dtype} {k} differs from ss_scan_bwd"
+        if i == 0:  # and against the fp64 oracle on the same inputs
+            oref = oracle_bwd(x, dy, True)
+            for k in NAMES:
+                check(to_host64(g[k]), oref[k], grad_kind(dtype, k in IO), f"noalloc {dtype} {k}")
 
 
 def test_noalloc_refuses_problems_larger_than_its_buffer():
