@@ -67,17 +67,39 @@ def build(force: bool = False, verbose: bool = False) -> str:
     build_probe(force)
     if not force and not stale():
         return SO
-    tmp = SO + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "--shared", "-Xcompiler", "-fPIC",
-           "--cudart", "shared", "-I", INCLUDE, "-o", tmp, *sources()]
+    # one object per source, compiled in parallel, then one link
+    from concurrent.futures import ThreadPoolExecutor
+    objdir = os.path.join(HERE, "_build")
+    os.makedirs(objdir, exist_ok=True)
+    flags = [*ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
     if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError("nvcc failed:\n" + r.stdout + r.stderr)
+        flags.append("-Xptxas=-v")
+
+    def compile_one(src):
+        obj = os.path.join(objdir, os.path.basename(src)[:-3] + f".{os.getpid()}.o")
+        r = subprocess.run([nvcc(), *flags, "-c", src, "-o", obj], capture_output=True, text=True)
+        return src, obj, r
+
+    with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
+        results = list(ex.map(compile_one, sources()))
+    errs = [src + ":\n" + r.stdout + r.stderr for src, _, r in results if r.returncode != 0]
     if verbose:
-        sys.stderr.write(r.stdout + r.stderr)
-    os.replace(tmp, SO)
+        for _, _, r in results:
+            sys.stderr.write(r.stdout + r.stderr)
+    objs = [obj for _, obj, _ in results]
+    try:
+        if errs:
+            raise RuntimeError("nvcc failed:\n" + "\n".join(errs))
+        tmp = SO + f".tmp{os.getpid()}"
+        r = subprocess.run([nvcc(), *ARCH, "--shared", "--cudart", "shared", "-o", tmp, *objs],
+                           capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("nvcc link failed:\n" + r.stdout + r.stderr)
+        os.replace(tmp, SO)
+    finally:
+        for obj in objs:
+            if os.path.exists(obj):
+                os.remove(obj)
     return SO
 
 
