@@ -1,36 +1,43 @@
 #!/usr/bin/env python
-"""Selective-scan bench: scanned elements per second (Bsz*Dch*L) of one
-training-and-decode pass of the whole hot path on one workload.
+"""Selective-scan bench: scanned elements per second (B*D*L) of the whole hot
+path, with the roofline of every kernel and the fp64 oracle timed beside it.
 
-One step = ss_scan_fwd (discretise, scan, contract, skip, gate) +
-ss_scan_bwd (its three stages: segment states, reverse pass, reduction) +
-one ss_step decode token continuing from the forward's final state (+ for
-N > 1 the all-reduce of dA, dD, ddelta_bias across replicas).
+Headline step (the JSON line's ``value``): one pass of the whole path over the
+Mamba-130M-shaped layer (Bsz=8, Dch=1536, L=2048, N=16, bf16 I/O, float32
+state): ss_scan_fwd + ss_scan_bwd (its three stages) + one ss_step decode
+token continuing from the forward's final state (+ for N > 1 replicas the
+all-reduce of dA, dD, ddelta_bias).  Synthetic seeded data with the
+workload's distributions (u, z, B, C, delta_raw, dy ~ N(0,1); A[d,n] =
+-(n+1); D ~ N(0,1); delta_bias = inverse softplus of dt, dt log-uniform in
+[1e-3, 1e-1]).
 
-Workload: the Mamba-130M-shaped layer Bsz=8, Dch=1536, L=2048, N=16 with bf16
-inputs/outputs and float32 state and accumulation; synthetic seeded data
-(u, z, B, C, delta_raw, dy ~ N(0,1); A[d,n] = -(n+1); D ~ N(0,1); delta_bias
-= inverse softplus of dt, dt log-uniform in [1e-3, 1e-1]).
+``configs`` in the line: each workload of the pages' configuration list with
+its own time, Gelem/s, roofline and fp64 oracle sample on the host cores --
+the Mamba-130M layer forward, the fp32 Mamba-370M layer forward + backward,
+the long-sequence forward (1 x 5120 x 131072) and the decode workload (128
+successive steps, 256 x 5120, state updated in place).
+
+Roofline counts follow the method, per scanned element (b, d, t), N states,
+s bytes per I/O element: forward 4N+10 FP32 operations and N+4 MUFU
+evaluations, backward 10N+10 and N+6 (the whole backward: the chunk
+summaries the kernels run first are part of its time, not extra work),
+bytes = each tensor read or written once.  The FP32 and MUFU peaks are per-SM
+rates measured by the microbenchmark built beside the library
+(``selective_state_space_114_b300/probe/pipes.cu``) times the SM count and
+the maximum SM clock; HBM is the measured copy bandwidth.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--no-cpu-baseline] [--pipes] [--profile-workload NAME]
 
-Prints one JSON line on rank 0.  ``--impl reference`` times the fp64 CPU
-oracle (the method as plain sequential code) on a bounded sample of the same
-workload on this machine's host cores.
-
-Besides the step, rank 0 adds side measurements to the line (each with its
-roofline): the decode step at Bsz=256, Dch=5120; conv1d + silu forward and
-backward; the tensor-core input projection (x_proj + dt_proj); the fp32
-Mamba-370M layer forward + backward; the long-sequence forward
-(1 x 5120 x 131072); the bench layer with 64 states; and a four-piece chunked
-prefill continued from the carried state.  ``--profile-workload`` runs only
-one workload's kernels, for an ncu capture.
+``--impl reference`` times the fp64 CPU oracle (the method as plain
+sequential code) on a bounded sample of the headline workload.  ``--pipes``
+prints the microbenchmark's rates and exits.  ``--profile-workload`` runs one
+workload's kernels a few times and exits, for an ncu capture.
 """
 from __future__ import annotations
 
 import argparse
-import hashlib
-import glob
+import ctypes
 import json
 import os
 import statistics
@@ -49,18 +56,16 @@ METRIC = "selective-scan Gelem/s (B·D·L), fwd and fwd+bwd; % of HBM/MUFU roofl
 UNIT = "Gelem/s"
 CFG_INDEX = 1
 N_STATE = 16
-
-# Hardware figures for the roofline denominators (one B300).
 SMS = 148
 SM_MAX_MHZ = 2032.0
-FP32_LANES = 128            # FP32 operations per clock per SM
-MUFU_LANES = 32             # MUFU (ex2 / lg2 / rcp) results per clock per SM, measured
-FP32_PEAK_T = SMS * FP32_LANES * SM_MAX_MHZ * 1e6 / 1e12   # 38.49 T ops/s
-MUFU_PEAK_T = SMS * MUFU_LANES * SM_MAX_MHZ * 1e6 / 1e12   # 9.62 T ops/s
 L2_BYTES = 126 * 2 ** 20
-# kernels one step launches: forward 1; backward states 2 (chunk summaries,
-# chunk carries), reverse 1, reduce 2 (dB/dC, dA/dD/dbias); decode step 1
+# kernels one headline step launches: forward 1; backward summaries 2 (chunk
+# summaries, chunk carries), reverse 1, reductions 2 (dB/dC, dA/dD/dbias);
+# decode step 1
 LAUNCHES_PER_STEP = 7
+# per-SM rates used when the microbenchmark cannot run (its last results on
+# this pool): FP32 operations, MUFU ex2 evaluations per SM clock
+FALLBACK_PIPES = {"ffma": 124.3, "ex2": 31.98}
 
 
 def load_peaks():
@@ -73,85 +78,110 @@ def load_peaks():
 
 
 # ---------------------------------------------------------------------------
-# Algorithmic work per scanned element (b, d, t) of each stage, N = 16,
-# s = bytes per I/O element, Dch = channels: what the method needs, not what
-# a kernel executes.  fp32 = FP32 add/mul/fma operations, mufu = exp / log /
-# reciprocal evaluations, bytes = each tensor read or written once.
-#   fwd:          per state: delta*A, delta*u*B, the state update, C*h (4N);
-#                 softplus 4, D skip 1, delta*u 1, gate 3; MUFU: N decays,
-#                 softplus 2, sigmoid 2.  Bytes: u, delta, z in, y out (4s)
-#                 plus B, C once per (b, t): 2Ns/Dch.
-#   bwd_states:   chunk summaries: per state delta*A, the input term, the
-#                 state fold, the decay product, yhat*C, the adjoint fold
-#                 (6N) + 12; MUFU N + 4.  Bytes: u, delta, z, dy in (4s) +
-#                 B, C + 33 floats out per 128 steps.
-#   bwd_reverse:  the backward proper: per state the recomputed decay and
-#                 state (3), adjoint (2), dC, dB, du-sum, ddelta-sum (2),
-#                 dA, pre-gate output (7) = 12N; + 20 per element; MUFU N + 6.
-#                 Bytes: u, delta, z, dy in, du, ddelta, dz out (7s), B, C,
-#                 dB, dC written once per (b, t): (2Ns + 8N)/Dch.
-#   bwd_reduce:   dB/dC partials of 128-row blocks read, dB, dC written:
-#                 2N*4*(ceil(Dch/128) + 1)/Dch.
+# pipe rates (microbenchmark) and peaks
 # ---------------------------------------------------------------------------
-def kernel_work(s, Dch, N=N_STATE):
-    G = (Dch + 127) // 128
-    return {
-        "fwd": dict(fp32=4 * N + 9, mufu=N + 4, bytes=4 * s + 2 * N * s / Dch),
-        "bwd_states": dict(fp32=6 * N + 12, mufu=N + 4,
-                           bytes=4 * s + 2 * N * s / Dch + 33 * 4 / 128),
-        "bwd_reverse": dict(fp32=12 * N + 20, mufu=N + 6,
-                            bytes=7 * s + (2 * N * s + 8 * N) / Dch),
-        "bwd_reduce": dict(fp32=0, mufu=0, bytes=2 * N * 4 * (G + 1) / Dch),
-    }
+PIPE_TESTS = {"ex2": 0, "lg2": 1, "rcp": 2, "ffma": 3, "ffma2": 4, "shfl": 5}
+# shared-memory access patterns: SM clocks per warp-wide access (wavefronts)
+SMEM_TESTS = {"ld128_uniform": 16, "ld128_quad_lane_mod4": 17, "ld128_lane_mod8": 18,
+              "ld128_adjacent_pairs": 19, "ld128_adjacent_quads": 20, "ld128_adjacent_octets": 21,
+              "ld128_distinct": 22, "ld64_uniform": 23, "ld64_distinct": 24, "ld32_uniform": 25,
+              "ld32_distinct": 26, "st128_distinct": 27, "ld128_two_halves": 28}
 
 
-def roofline(name, work, elems, ms, hbm_gbs, traffic=None):
-    """Roofline of one kernel: the binding resource is the one whose
-    algorithmic work takes longest at its peak; achieved = that work / the
-    measured time."""
+def measure_pipes(warps=16, iters=4096, tests=PIPE_TESTS):
+    """Per-SM rates from the pipe microbenchmark (one CTA per SM, fixed trip
+    counts, the SM cycle counter around the loop): lane results per SM clock
+    for the ALU tests, SM clocks per warp-wide access for the shared-memory
+    ones.  Returns {name: rate} or None when the probe library is unavailable."""
+    so = os.path.join(ROOT, "selective_state_space_114_b300", "libssprobe.so")
+    if not os.path.exists(so):
+        return None
+    lib = ctypes.CDLL(so)
+    lib.ssp_run.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                            ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
+    out = {}
+    for name, t in tests.items():
+        c, r = ctypes.c_double(), ctypes.c_double()
+        for _ in range(2):  # the first run loads the module
+            if lib.ssp_run(t, warps, iters if t < 16 else iters // 4, ctypes.byref(c),
+                           ctypes.byref(r)) != 0:
+                return None
+        out[name] = round(r.value, 3)
+    return out
+
+
+class Peaks:
+    """Roofline denominators: FP32 and MUFU from per-SM rates x SMs x the
+    maximum SM clock, HBM from the measured copy bandwidth."""
+
+    def __init__(self, pipes=None):
+        self.hbm_gbs, self.hbm_src = load_peaks()
+        self.pipes_src = "measured" if pipes else "fallback"
+        pipes = pipes or FALLBACK_PIPES
+        self.fp32_per_clk = pipes["ffma"]
+        self.mufu_per_clk = pipes["ex2"]
+        self.fp32_t = SMS * self.fp32_per_clk * SM_MAX_MHZ * 1e6 / 1e12
+        self.mufu_t = SMS * self.mufu_per_clk * SM_MAX_MHZ * 1e6 / 1e12
+        self.pipes = pipes
+
+    def describe(self):
+        return {"hbm_gbs": self.hbm_gbs, "hbm": self.hbm_src,
+                "fp32_tops": round(self.fp32_t, 2), "mufu_tops": round(self.mufu_t, 3),
+                "pipes": self.pipes_src, "per_sm_clk": self.pipes,
+                "clock_mhz": SM_MAX_MHZ, "sms": SMS}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work of the method (per scanned element)
+# ---------------------------------------------------------------------------
+def method_work(kind, s, Dch, N=N_STATE, Bsz=1):
+    """Per scanned element (b, d, t) for kind in fwd, bwd, fwd_bwd; per token
+    row (b, d) for step.  fp32 = FP32 add/mul/fma operations, mufu = exp / log
+    / reciprocal evaluations, bytes = each tensor read or written once (B, C,
+    dB, dC once per (b, t), parameters once).
+      fwd:  per state delta*A, delta*u*B, the state update, C*h (4N); softplus
+            4, D skip 1, delta*u 1, gate 3, the state sum 1; MUFU: N decays,
+            softplus 2, sigmoid 2.  Bytes: u, delta, z in, y out, B and C.
+      bwd:  (14N + 20) for forward and backward together, less the forward's
+            4N + 10; MUFU N + 6.  Bytes: u, delta, z, dy in; du, ddelta, dz
+            out; B, C in; dB, dC out (float32).
+      step: a forward element with the state read and written (float32).
+    """
+    fwd = dict(fp32=4 * N + 10, mufu=N + 4, bytes=4 * s + 2 * N * s / Dch)
+    bwd = dict(fp32=10 * N + 10, mufu=N + 6, bytes=7 * s + (2 * N * s + 8 * N) / Dch)
+    if kind == "fwd":
+        return fwd
+    if kind == "bwd":
+        return bwd
+    if kind == "fwd_bwd":
+        return {k: fwd[k] + bwd[k] for k in fwd}
+    if kind == "step":
+        return dict(fp32=4 * N + 10, mufu=N + 4, bytes=8 * N + 4 * s + 2 * N * s / Dch)
+    raise ValueError(kind)
+
+
+def roofline(work, units, ms, peaks, traffic=None):
+    """The binding resource is the one whose algorithmic work takes longest at
+    its peak; achieved = that work / the measured time."""
     t = ms * 1e-3
-    times = {"hbm": work["bytes"] * elems / (hbm_gbs * 1e9),
-             "fp32": work["fp32"] * elems / (FP32_PEAK_T * 1e12),
-             "mufu": work["mufu"] * elems / (MUFU_PEAK_T * 1e12)}
+    times = {"hbm": work["bytes"] * units / (peaks.hbm_gbs * 1e9),
+             "fp32": work["fp32"] * units / (peaks.fp32_t * 1e12),
+             "mufu": work["mufu"] * units / (peaks.mufu_t * 1e12)}
     res = max(times, key=times.get)
-    base = {"kernel": name, "traffic": traffic, "resource": res,
-            "algorithmic_bytes": work["bytes"] * elems, "algorithmic_fp32": work["fp32"] * elems,
-            "algorithmic_mufu": work["mufu"] * elems,
-            "bound_ms": {k: round(v * 1e3, 4) for k, v in times.items()}}
     if res == "hbm":
-        ach = work["bytes"] * elems / t / 1e9
-        return {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_gbs, "unit": "GB/s",
-                "frac": round(ach / hbm_gbs, 4), **base}
-    peak = FP32_PEAK_T if res == "fp32" else MUFU_PEAK_T
-    ach = work[res] * elems / t / 1e12
-    return {"bound": "alu", "achieved": round(ach, 3), "peak": round(peak, 3), "unit": "TFLOP/s",
-            "frac": round(ach / peak, 4), **base}
-
-
-# The sources the step's kernels (forward, backward, decode token) are built
-# from: ncu traffic taken on other versions of these files is not reported.
-STEP_SOURCES = ("common.cuh", "launch.h", "scan_fwd.cu", "scan_bwd.cu", "step.cu")
-
-
-def csrc_digest():
-    h = hashlib.sha256()
-    for name in STEP_SOURCES:
-        h.update(open(os.path.join(ROOT, "selective_state_space_114_b300", "csrc", name), "rb").read())
-    return h.hexdigest()[:16]
-
-
-def ncu_traffic(kernel):
-    """DRAM bytes per launch from the committed ncu summary, when it was
-    taken on the current kernel sources; else None."""
-    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
-    try:
-        d = json.load(open(p))
-    except Exception:
-        return None
-    if d.get("csrc_digest") != csrc_digest():
-        return None
-    v = d.get("kernels", {}).get(kernel)
-    return None if v is None else v.get("dram_bytes_per_launch")
+        ach = work["bytes"] * units / t / 1e9
+        out = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks.hbm_gbs, "unit": "GB/s"}
+        frac = ach / peaks.hbm_gbs
+    else:
+        peak = peaks.fp32_t if res == "fp32" else peaks.mufu_t
+        ach = work[res] * units / t / 1e12
+        out = {"bound": "alu", "resource": res, "achieved": round(ach, 3),
+               "peak": round(peak, 3), "unit": "TFLOP/s"}
+        frac = ach / peak
+    out["frac"] = round(frac, 4)
+    out["traffic"] = traffic
+    out["bound_ms"] = round(times[res] * 1e3, 4)
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -291,71 +321,73 @@ def dist_env():
 
 def workload_config(world):
     cfg = synth.config(CFG_INDEX)
-    E = cfg["Bsz"] * cfg["Dch"] * cfg["L"]
-    per_step_mb = (8 * E * 2 + 8 * E * 2) / 2 ** 20
     return cfg, {
-        "workload": "mamba130m-shaped selective-scan layer: Bsz=8 Dch=1536 L=2048 N=16, bf16 "
-                    "I/O, f32 state; step = fwd + bwd (3 stages) + 1 decode token",
+        "workload": "mamba130m-shaped layer 8x1536x2048 N=16: fwd + bwd + 1 decode token",
         "Bsz": cfg["Bsz"], "Dch": cfg["Dch"], "L": cfg["L"], "N": cfg["N"], "io_dtype": "bf16",
-        "softplus": True, "gate": True, "global_batch": cfg["Bsz"] * world,
+        "global_batch": cfg["Bsz"] * world,
         "parallelism": "replicas" if world == 1 else f"dp{world} (param-grad all-reduce)",
-        "l2": f"inputs larger than L2: ~{per_step_mb:.0f} MiB of activations and gradients "
-              f"touched per step vs {L2_BYTES // 2**20} MiB L2; no flush",
+        "l2": "no flush: ~770 MiB of activations and gradients per step, 6x L2",
     }
 
 
 # ---------------------------------------------------------------------------
 # CPU (oracle) timing
 # ---------------------------------------------------------------------------
-def oracle_sample_step(cfg, nch, seed):
-    """One fp64 oracle pass (fwd + bwd + one step) over all Bsz batches of
-    the first ``nch`` channels, L = full length.  Returns seconds."""
+def _host(cfg, n, seed, with_dy=False):
+    """Host inputs of a workload cut to n channels (same distributions),
+    widened exactly to float64."""
+    x = synth.make_inputs(dict(cfg, Dch=n), seed=seed, with_dy=with_dy)
+    return {k: synth.widen(v) for k, v in x.items()}
+
+
+def oracle_pass(kind, cfg, n, seed):
+    """One fp64 oracle pass over all batches x n channels x the full length
+    (kind fwd, fwd_bwd or step: fwd + bwd + one decode token; decode: the
+    configured number of successive steps over Bsz x n rows).  Returns
+    (seconds, scanned elements)."""
     import oracle
-    sub = dict(cfg, Dch=nch)
-    x = synth.make_inputs(sub, seed=seed, with_dy=True)
-    w = {k: synth.widen(v) for k, v in x.items()}
+    if kind == "decode":
+        sub = dict(cfg, Dch=n, L=1)
+        x = _host(sub, n, seed)
+        toks = [{k: synth.widen(v) for k, v in synth.step_inputs(sub, k, seed=seed).items()}
+                for k in range(cfg["steps"])]
+        h = np.zeros((cfg["Bsz"], n, cfg["N"]))
+        t0 = time.perf_counter()
+        for tk in toks:
+            _, h = oracle.step(h, tk["u"], tk["delta"], x["A"], tk["B"], tk["C"], x["D"], tk["z"],
+                               x["delta_bias"], True)
+        return time.perf_counter() - t0, cfg["Bsz"] * n * cfg["steps"]
+    w = _host(cfg, n, seed, with_dy=kind != "fwd")
     t0 = time.perf_counter()
     _, h = oracle.scan_fwd(w["u"], w["delta"], w["A"], w["B"], w["C"], w["D"], w["z"],
                            w["delta_bias"], True)
-    oracle.scan_bwd(w["u"], w["delta"], w["A"], w["B"], w["C"], w["D"], w["z"],
-                    w["delta_bias"], True, w["dy"])
-    tok = synth.step_inputs(dict(sub, L=1), 0, seed=seed)
-    tw = {k: synth.widen(v) for k, v in tok.items()}
-    oracle.step(h, tw["u"], tw["delta"], w["A"], tw["B"], tw["C"], w["D"], tw["z"],
-                w["delta_bias"], True)
-    return time.perf_counter() - t0
+    if kind != "fwd":
+        oracle.scan_bwd(w["u"], w["delta"], w["A"], w["B"], w["C"], w["D"], w["z"],
+                        w["delta_bias"], True, w["dy"])
+    if kind == "step":
+        sub = dict(cfg, Dch=n, L=1)
+        tk = {k: synth.widen(v) for k, v in synth.step_inputs(sub, 0, seed=seed).items()}
+        oracle.step(h, tk["u"], tk["delta"], w["A"], tk["B"], tk["C"], w["D"], tk["z"],
+                    w["delta_bias"], True)
+    return time.perf_counter() - t0, cfg["Bsz"] * n * cfg["L"]
 
 
-def size_oracle_sample(cfg, target_s, seed):
-    """Number of channels (all batches, full L) whose oracle pass takes about
-    target_s seconds on the host cores (capped at the whole workload)."""
-    cores = os.cpu_count() or 1
-    n = max(2, min(cores, 8))
-    for _ in range(4):
-        t = oracle_sample_step(cfg, n, seed)
+def oracle_sample(kind, cfg, seed, target_s):
+    """The oracle as it stands on the host cores, on about target_s seconds of
+    the workload (whole channels, all batches, full length), sized by doubling
+    the channel count."""
+    import oracle
+    n = min(cfg["Dch"], 2)
+    while True:
+        t, e = oracle_pass(kind, cfg, n, seed)
         if t >= 0.5 * target_s or n >= cfg["Dch"]:
             break
-        n = int(min(cfg["Dch"], max(2 * n, n * target_s / max(t, 1e-6))))
-    return n
-
-
-def cpu_baseline(cfg, seed, target_s=12.0):
-    """The oracle as it stands, timed on the host cores: passes over the
-    first n channels (all batches, full L), repeated while the sample is
-    shorter than about target_s seconds."""
-    import oracle
-    cores = oracle.default_threads()
-    n = size_oracle_sample(cfg, target_s, seed)
-    t = oracle_sample_step(cfg, n, seed)
-    reps = 1
-    while t < 0.5 * target_s and reps < 64:
-        t += oracle_sample_step(cfg, n, seed)
-        reps += 1
-    elems = cfg["Bsz"] * n * cfg["L"] * reps
-    return {"value": round(elems / t / 1e9, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{reps} fp64 oracle pass(es) of fwd+bwd+1 step over all {cfg['Bsz']} "
-                      f"batches x first {n} of {cfg['Dch']} channels x L={cfg['L']} "
-                      f"({elems} elements, {t:.1f} s)"}
+        n = int(min(cfg["Dch"], max(n + 1, n * min(8.0, target_s / max(t, 1e-3)))))
+    steps = f"{cfg['steps']} steps of " if kind == "decode" else ""
+    return {"value": round(e / t / 1e9, 6), "unit": UNIT, "cores": oracle.default_threads(),
+            "kind": "oracle", "sample": f"fp64 {kind}: {steps}{cfg['Bsz']} x {n} of {cfg['Dch']} "
+                                        f"channels x L={cfg['L']} ({e} el, {t:.1f} s)",
+            "short": f"{steps}{cfg['Bsz']}x{n}x{cfg['L']}, {t:.1f} s"}
 
 
 def run_reference(args):
@@ -366,152 +398,66 @@ def run_reference(args):
     import oracle
     cores = oracle.default_threads()
     W, K = max(3, args.warmup), args.steps
-    budget = 150.0  # seconds for the whole run
-    per_step = max(0.5, budget / (W + K))
-    n = size_oracle_sample(cfg, per_step, cfg["seed"])
+    per_step = max(0.5, 150.0 / (W + K))  # the whole run in about 150 s
+    n = 2
+    while True:
+        t, e = oracle_pass("step", cfg, n, cfg["seed"])
+        if t >= 0.5 * per_step or n >= cfg["Dch"]:
+            break
+        n = int(min(cfg["Dch"], max(n + 1, n * per_step / max(t, 1e-3))))
     for _ in range(W):
-        oracle_sample_step(cfg, n, cfg["seed"])
-    times = [oracle_sample_step(cfg, n, cfg["seed"]) for _ in range(K)]
+        oracle_pass("step", cfg, n, cfg["seed"])
+    times = [oracle_pass("step", cfg, n, cfg["seed"])[0] for _ in range(K)]
     elems = cfg["Bsz"] * n * cfg["L"]
     ms = 1e3 * sum(times) / K
     value = elems / (ms * 1e-3) / 1e9
-    line = {
+    sample = (f"each step: fp64 oracle fwd + bwd + 1 decode token over {cfg['Bsz']} x {n} of "
+              f"{cfg['Dch']} channels x L={cfg['L']} ({elems} elements)")
+    print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
         "n_gpus": args.gpus, "steps": K, "warmup": W, "ms_per_step": round(ms, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": conf,
-        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"each step: fp64 oracle fwd+bwd+1 decode step over all "
-                                   f"{cfg['Bsz']} batches x first {n} of {cfg['Dch']} channels x "
-                                   f"L={cfg['L']} ({elems} elements)"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores,
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
-                "d2h_bytes_per_step": 0},
-    }
-    print(json.dumps(line), flush=True)
+                "d2h_bytes_per_step": 0}}), flush=True)
     return 0
 
 
 # ---------------------------------------------------------------------------
 # GPU timing
 # ---------------------------------------------------------------------------
-def _flushed_median_ms(fn, steps, dev):
-    """Median time of fn() with L2 flushed before each call (a 256 MiB read).
-    The GPU first spins for ~25 ms so that the host enqueues every timed call
-    ahead of it: the events then bracket GPU work only, not launch latency."""
+def _timed_ms(fns, steps, dev, flush=False):
+    """Mean device time of each function over `steps` rounds after 3 warm-up
+    rounds.  The GPU first spins (~25 ms) so that the host has enqueued every
+    timed launch before the first runs.  flush: a 256 MiB read before each
+    round empties L2 of the round's data (for workloads smaller than L2)."""
     import torch
-    flush = torch.ones(64 * 2 ** 20, device=dev, dtype=torch.float32)
+    buf = torch.ones(64 * 2 ** 20, device=dev, dtype=torch.float32) if flush else None
     sink = torch.empty((), device=dev, dtype=torch.float32)
     for _ in range(3):
-        fn()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        for f in fns:
+            f()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)]
            for _ in range(steps)]
     torch.cuda.synchronize()
     torch.cuda._sleep(50_000_000)
-    for e0, e1 in evs:
-        torch.sum(flush, dim=0, out=sink)
-        e0.record()
-        fn()
-        e1.record()
+    for row in evs:
+        if buf is not None:
+            torch.sum(buf, dim=0, out=sink)
+        row[0].record()
+        for i, f in enumerate(fns):
+            f()
+            row[i + 1].record()
     torch.cuda.synchronize()
-    return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
-
-
-def conv_measure(ss, dev, seed, steps=16):
-    """The causal depthwise conv1d + silu (width 4) that produces u, forward
-    and backward, on the bench layer's shape (8 x 1536 x 2048, bf16); L2 is
-    flushed before each call.  Returns times and HBM rooflines."""
-    import torch
-    cfg = synth.config(CFG_INDEX)
-    Bsz, Dch, L, K = cfg["Bsz"], cfg["Dch"], cfg["L"], 4
-    E = Bsz * Dch * L
-    bf = torch.bfloat16
-    x = torch.from_numpy(synth.normal(seed, 20, E, "bf16").reshape(Bsz, Dch, L)).view(bf).to(dev)
-    g = torch.from_numpy(synth.normal(seed, 23, E, "bf16").reshape(Bsz, Dch, L)).view(bf).to(dev)
-    w = torch.from_numpy(synth.normal(seed, 21, Dch * K, "f32").reshape(Dch, K) / 2.0).to(dev)
-    b = torch.from_numpy(synth.normal(seed, 22, Dch, "f32")).to(dev)
-    u = torch.empty_like(x)
-    grads = {"dx": torch.empty_like(x), "dw": torch.empty((Dch, K), device=dev),
-             "dbias": torch.empty((Dch,), device=dev)}
-    ms_f = _flushed_median_ms(lambda: ss.ss_conv1d_silu(x, w, b, True, out=u), steps, dev)
-    ms_b = _flushed_median_ms(lambda: ss.ss_conv1d_silu_bwd(x, w, b, True, g, out=grads), steps,
-                              dev)
-    hbm, _ = load_peaks()
-    res = {"workload": f"conv1d (width {K}) + silu, Bsz={Bsz} Dch={Dch} L={L}, bf16, "
-                       f"L2 flushed before each call"}
-    for name, ms, nbytes in (("fwd", ms_f, 2 * 2 * E), ("bwd", ms_b, 3 * 2 * E)):
-        ach = nbytes / (ms * 1e-3) / 1e9
-        res[name] = {"ms": round(ms, 4), "gelem_s": round(E / (ms * 1e-3) / 1e9, 2), "bound": "hbm",
-                     "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(ach / hbm, 4), "algorithmic_bytes": nbytes}
-    return res
-def xproj_measure(ss, dev, seed, steps=16):
-    """The input projection (x_proj then dt_proj on the tensor cores) on the
-    bench layer's shape (8 x 1536 x 2048, dt_rank 48, N = 16, bf16), L2
-    flushed before each call.  HBM-bound: u read, delta, B, C written."""
-    import torch
-    cfg = synth.config(CFG_INDEX)
-    Bsz, Dch, L, N, R = cfg["Bsz"], cfg["Dch"], cfg["L"], cfg["N"], 48
-    E = Bsz * Dch * L
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(seed)
-    bf = torch.bfloat16
-    u = torch.randn((Bsz, Dch, L), generator=gen, device=dev).to(bf)
-    Wx = (torch.randn((R + 2 * N, Dch), generator=gen, device=dev) / Dch ** 0.5).to(bf)
-    Wdt = (torch.randn((Dch, R), generator=gen, device=dev) / R ** 0.5).to(bf)
-    out = (torch.empty_like(u), torch.empty((Bsz, N, L), device=dev, dtype=bf),
-           torch.empty((Bsz, N, L), device=dev, dtype=bf))
-    ms = _flushed_median_ms(lambda: ss.ss_xproj(u, Wx, Wdt, N, out=out), steps, dev)
-    nbytes = 2 * E * 2 + 2 * 2 * Bsz * N * L + 2 * (R + 2 * N) * Dch + 2 * Dch * R
-    flops = 2 * Bsz * L * Dch * (R + 2 * N) + 2 * Bsz * L * R * Dch
-    hbm, _ = load_peaks()
-    ach = nbytes / (ms * 1e-3) / 1e9
-    return {"workload": f"x_proj + dt_proj, Bsz={Bsz} Dch={Dch} L={L} dt_rank={R} N={N}, bf16, "
-                        f"L2 flushed before each call",
-            "ms": round(ms, 4), "bound": "hbm", "achieved": round(ach, 1), "peak": hbm,
-            "unit": "GB/s", "frac": round(ach / hbm, 4), "algorithmic_bytes": nbytes,
-            "tensor_tflops": round(flops / (ms * 1e-3) / 1e12, 2),
-            "wait_failures": ss.ss_xproj_wait_failures()}
-
-
-def decode_step_measure(ss, dev, seed, steps=16):
-    """The one-token step on the decode workload (Bsz=256, Dch=5120, N=16,
-    bf16 tokens, float32 state): its state (84 MB) fits in L2, so L2 is
-    flushed before each timed step by reading a 256 MiB buffer (a read leaves
-    no dirty lines to be written back during the step); the events bracket
-    the step kernel only.  Returns its time and HBM roofline."""
-    import torch
-    cfg = synth.config(4)
-    Bsz, Dch, N = cfg["Bsz"], cfg["Dch"], cfg["N"]
-    x = synth.make_inputs(dict(cfg, L=1), seed=seed)
-    tok = synth.step_inputs(cfg, 0, seed=seed)
-    bf = torch.bfloat16
-
-    def t(a):
-        return torch.from_numpy(np.ascontiguousarray(a)).view(bf).to(dev)
-
-    u, dl, z, B, C = (t(tok[k]) for k in ("u", "delta", "z", "B", "C"))
-    A = torch.from_numpy(np.ascontiguousarray(x["A"], dtype=np.float32)).to(dev)
-    D = torch.from_numpy(np.ascontiguousarray(x["D"], dtype=np.float32)).to(dev)
-    bias = torch.from_numpy(np.ascontiguousarray(x["delta_bias"], dtype=np.float32)).to(dev)
-    h = torch.zeros((Bsz, Dch, N), device=dev, dtype=torch.float32)
-    y = torch.empty((Bsz, Dch), device=dev, dtype=bf)
-    ms = _flushed_median_ms(lambda: ss.ss_step(h, u, dl, A, B, C, D, z, bias, True, out=y), steps,
-                            dev)
-    rows = Bsz * Dch
-    nbytes = rows * (2 * N * 4 + 4 * 2) + 2 * Bsz * N * 2  # h in/out, u/delta/z/y, B/C
-    hbm, _ = load_peaks()
-    ach = nbytes / (ms * 1e-3) / 1e9
-    return {"workload": f"decode step Bsz={Bsz} Dch={Dch} N={N}, bf16 tokens, f32 state, "
-                        f"L2 flushed before each step", "ms": round(ms, 4),
-            "bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
-            "frac": round(ach / hbm, 4), "algorithmic_bytes": nbytes}
+    return [statistics.mean(r[i].elapsed_time(r[i + 1]) for r in evs) for i in range(len(fns))]
 
 
 def _device_inputs(cfg, dev, seed, with_dy=False):
-    """Inputs of a workload made on the device: activations and B/C drawn from
-    N(0, 1) by torch's seeded generator (the workload's distributions, not the
-    host generator's values; timing does not depend on them), A, D and
-    delta_bias from the host generator."""
+    """Inputs drawn on the device by torch's seeded generator with the
+    workload's distributions (timing does not depend on the values); A, D
+    and delta_bias from the host generator."""
     import torch
     Bsz, Dch, L, N = cfg["Bsz"], cfg["Dch"], cfg["L"], cfg["N"]
     dtype = torch.bfloat16 if cfg["dtype"] == "bf16" else torch.float32
@@ -531,165 +477,207 @@ def _device_inputs(cfg, dev, seed, with_dy=False):
     return x, dtype
 
 
-def _timed_ms(fns, steps, dev):
-    """Mean device time of each function in fns over `steps` back-to-back
-    rounds (inputs far larger than L2, so no flush), after 3 warm-up rounds."""
+def _grads(x, dev):
     import torch
-    for _ in range(3):
-        for f in fns:
-            f()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)]
-           for _ in range(steps)]
-    torch.cuda.synchronize()
-    torch.cuda._sleep(50_000_000)
-    for row in evs:
-        row[0].record()
-        for i, f in enumerate(fns):
-            f()
-            row[i + 1].record()
-    torch.cuda.synchronize()
-    return [statistics.mean(r[i].elapsed_time(r[i + 1]) for r in evs) for i in range(len(fns))]
+    Bsz, Dch, L = x["u"].shape
+    N = x["A"].shape[1]
+    return {"du": torch.empty_like(x["u"]), "ddelta": torch.empty_like(x["u"]),
+            "dz": torch.empty_like(x["u"]), "dA": torch.empty((Dch, N), device=dev),
+            "dB": torch.empty((Bsz, N, L), device=dev), "dC": torch.empty((Bsz, N, L), device=dev),
+            "dD": torch.empty((Dch,), device=dev), "ddelta_bias": torch.empty((Dch,), device=dev)}
 
 
-def configs_measure(ss, dev, seed):
-    """The other full-size workloads: the fp32 Mamba-370M-shaped layer forward
-    and backward (8 x 2048 x 2048) and the long-sequence bf16 forward
-    (1 x 5120 x 131072), each kernel stage with its roofline."""
+BWD_STAGES = ("ss_scan_bwd_states", "ss_scan_bwd_reverse", "ss_scan_bwd_reduce")
+
+
+def _r(d):
+    """The roofline keys a config entry keeps: the binding resource and the
+    fraction of its peak (the peaks are in the line's "peaks")."""
+    return {"bound": d.get("resource", d["bound"]), "frac": d["frac"]}
+
+
+def config_lines(ss, dev, seed, peaks, cpu=True):
+    """One entry per workload of the configuration list: time, Gelem/s,
+    roofline (method counts), and the oracle on a bounded sample."""
     import torch
-    hbm, _ = load_peaks()
     out = {}
+    # Mamba-130M-shaped layer, forward (bf16)
+    cfg = synth.config(1)
+    x, _ = _device_inputs(cfg, dev, seed + 1)
+    E = cfg["Bsz"] * cfg["Dch"] * cfg["L"]
+    args = (x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], True)
+    y = torch.empty_like(x["u"])
+    (t,) = _timed_ms([lambda: ss.ss_scan_fwd(*args, out=y)], 20, dev)
+    out["mamba130m_fwd"] = {"ms": round(t, 4),
+                            "gelem_s": round(E / t / 1e6, 2),
+                            **_r(roofline(method_work("fwd", 2, cfg["Dch"]), E, t, peaks))}
+    del x, y
+    # Mamba-370M-shaped layer, forward + backward (fp32)
     cfg = synth.config(2)
-    x, dtype = _device_inputs(cfg, dev, seed + 2, with_dy=True)
+    x, _ = _device_inputs(cfg, dev, seed + 2, with_dy=True)
     Bsz, Dch, L, N = cfg["Bsz"], cfg["Dch"], cfg["L"], cfg["N"]
     E = Bsz * Dch * L
-    y = torch.empty_like(x["u"])
-    g = {"du": torch.empty_like(y), "ddelta": torch.empty_like(y), "dz": torch.empty_like(y),
-         "dA": torch.empty((Dch, N), device=dev), "dB": torch.empty((Bsz, N, L), device=dev),
-         "dC": torch.empty((Bsz, N, L), device=dev), "dD": torch.empty((Dch,), device=dev),
-         "ddelta_bias": torch.empty((Dch,), device=dev)}
+    args = (x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], True)
+    y, g = torch.empty_like(x["u"]), _grads(x, dev)
     ws = torch.empty(ss.ss_scan_bwd_workspace_size(Bsz, Dch, L, N, ss.SS_F32), device=dev,
                      dtype=torch.uint8)
-    args = (x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], True)
-    fns = [lambda: ss.ss_scan_fwd(*args, out=y)]
-    names = ["fwd", "bwd_states", "bwd_reverse", "bwd_reduce"]
-    for st in ("ss_scan_bwd_states", "ss_scan_bwd_reverse", "ss_scan_bwd_reduce"):
-        fns.append(lambda st=st: ss.ss_scan_bwd(*args, x["dy"], workspace=ws, out=g,
-                                                stages=(st,)))
+    fns = [lambda: ss.ss_scan_fwd(*args, out=y)] + [
+        lambda st=st: ss.ss_scan_bwd(*args, x["dy"], workspace=ws, out=g, stages=(st,))
+        for st in BWD_STAGES]
     ms = _timed_ms(fns, 10, dev)
-    work = kernel_work(4, Dch)
-    tot = sum(ms)
-    out["mamba370m_fp32_fwd_bwd"] = {
-        "workload": f"Bsz={Bsz} Dch={Dch} L={L} N={N}, fp32 I/O, fwd + bwd, inputs larger than L2",
-        "gelem_s": round(E / (tot * 1e-3) / 1e9, 3), "ms": round(tot, 4),
-        "kernels": {nm: {"ms": round(t, 4), **{k: v for k, v in roofline(nm, work[nm], E, t, hbm)
-                                               .items() if k in ("bound", "achieved", "peak",
-                                                                 "unit", "frac", "resource")}}
-                    for nm, t in zip(names, ms)}}
+    tb = sum(ms[1:])
+    out["mamba370m_fwd_bwd"] = {
+        "ms": round(sum(ms), 4),
+        "gelem_s": round(E / sum(ms) / 1e6, 2),
+        **_r(roofline(method_work("fwd_bwd", 4, Dch), E, sum(ms), peaks)),
+        "fwd": {"ms": round(ms[0], 4), "frac": roofline(method_work("fwd", 4, Dch), E, ms[0],
+                                                        peaks)["frac"]},
+        "bwd": {"ms": round(tb, 4), "frac": roofline(method_work("bwd", 4, Dch), E, tb,
+                                                     peaks)["frac"],
+                "stages": [round(v, 4) for v in ms[1:]]}}
     del x, y, g, ws
     torch.cuda.empty_cache()
-
+    # long sequence, forward (bf16)
     cfg = synth.config(3)
-    x, dtype = _device_inputs(cfg, dev, seed + 3)
-    Bsz, Dch, L, N = cfg["Bsz"], cfg["Dch"], cfg["L"], cfg["N"]
-    E = Bsz * Dch * L
-    y = torch.empty_like(x["u"])
-    h = torch.empty((Bsz, Dch, N), device=dev)
+    x, _ = _device_inputs(cfg, dev, seed + 3)
+    E = cfg["Bsz"] * cfg["Dch"] * cfg["L"]
     args = (x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], True)
+    y = torch.empty_like(x["u"])
+    h = torch.empty((cfg["Bsz"], cfg["Dch"], cfg["N"]), device=dev)
     (t,) = _timed_ms([lambda: ss.ss_scan_fwd(*args, out=y, h_last=h, return_last_state=True)],
                      5, dev)
-    r = roofline("fwd", kernel_work(2, Dch)["fwd"], E, t, hbm)
-    out["long_sequence_bf16_fwd"] = {
-        "workload": f"Bsz={Bsz} Dch={Dch} L={L} N={N}, bf16 I/O, f32 state, fwd, "
-                    f"inputs larger than L2",
-        "gelem_s": round(E / (t * 1e-3) / 1e9, 3), "ms": round(t, 4),
-        **{k: v for k, v in r.items() if k in ("bound", "achieved", "peak", "unit", "frac",
-                                               "resource")}}
+    out["long_sequence_fwd"] = {"ms": round(t, 4),
+                                "gelem_s": round(E / t / 1e6, 2),
+                                **_r(roofline(method_work("fwd", 2, cfg["Dch"]), E, t, peaks))}
     del x, y, h
     torch.cuda.empty_cache()
-
-    # the bench layer (8 x 1536 x 2048, bf16) with 64 states, forward and backward
-    cfg = dict(synth.config(1), N=64)
-    x, dtype = _device_inputs(cfg, dev, seed + 5, with_dy=True)
-    Bsz, Dch, L, N = cfg["Bsz"], cfg["Dch"], cfg["L"], cfg["N"]
-    E = Bsz * Dch * L
-    y = torch.empty_like(x["u"])
-    ws = torch.empty(ss.ss_scan_bwd_workspace_size(Bsz, Dch, L, N, ss.SS_BF16), device=dev,
-                     dtype=torch.uint8)
-    args = (x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], True)
-    g = ss.ss_scan_bwd(*args, x["dy"], workspace=ws)
-    fns = [lambda: ss.ss_scan_fwd(*args, out=y)]
-    for st in ("ss_scan_bwd_states", "ss_scan_bwd_reverse", "ss_scan_bwd_reduce"):
-        fns.append(lambda st=st: ss.ss_scan_bwd(*args, x["dy"], workspace=ws, out=g,
-                                                stages=(st,)))
-    ms = _timed_ms(fns, 5, dev)
-    work = kernel_work(2, Dch, N)
-    out["state_size_64_bf16_fwd_bwd"] = {
-        "workload": f"Bsz={Bsz} Dch={Dch} L={L} N={N}, bf16 I/O, fwd + bwd, inputs larger than L2",
-        "gelem_s": round(E / (sum(ms) * 1e-3) / 1e9, 3), "ms": round(sum(ms), 4),
-        "kernels": {nm: {"ms": round(t, 4), **{k: v for k, v in roofline(nm, work[nm], E, t, hbm)
-                                               .items() if k in ("bound", "achieved", "peak",
-                                                                 "unit", "frac", "resource")}}
-                    for nm, t in zip(["fwd", "bwd_states", "bwd_reverse", "bwd_reduce"], ms)}}
-    del x, y, g, ws
-    torch.cuda.empty_cache()
-
-    # chunked prefill: the bench layer's forward as four 512-step pieces, each
-    # continuing from the state the previous one left (updated in place)
-    cfg = synth.config(1)
-    x, dtype = _device_inputs(cfg, dev, seed + 6)
-    Bsz, Dch, L, N = cfg["Bsz"], cfg["Dch"], cfg["L"], cfg["N"]
-    E = Bsz * Dch * L
-    P = 4
-    Lp = L // P
-    pieces = [{k: x[k][..., i * Lp:(i + 1) * Lp].contiguous() for k in ("u", "delta", "z", "B",
-                                                                       "C")}
-              for i in range(P)]
-    ys = [torch.empty_like(pc["u"]) for pc in pieces]
+    # decode: 128 successive tokens, the state updated in place (L2 flushed
+    # before each run of 128; within a run the 84 MB state may stay in L2)
+    cfg = synth.config(4)
+    Bsz, Dch, N, S = cfg["Bsz"], cfg["Dch"], cfg["N"], cfg["steps"]
+    x, _ = _device_inputs(dict(cfg, L=1), dev, seed + 4)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed + 40)
+    bf = torch.bfloat16
+    toks = [{k: torch.randn(shp, generator=gen, device=dev).to(bf) for k, shp in
+             (("u", (Bsz, Dch)), ("delta", (Bsz, Dch)), ("z", (Bsz, Dch)), ("B", (Bsz, N)),
+              ("C", (Bsz, N)))} for _ in range(S)]
     h = torch.zeros((Bsz, Dch, N), device=dev)
+    ys = torch.empty((S, Bsz, Dch), device=dev, dtype=bf)
 
-    def prefill():
-        for i, pc in enumerate(pieces):
-            ss.ss_scan_fwd(pc["u"], pc["delta"], x["A"], pc["B"], pc["C"], x["D"], pc["z"],
-                           x["delta_bias"], True, out=ys[i], return_last_state=True,
-                           h0=h if i else None, h_last=h)
+    def run128():
+        for i, tk in enumerate(toks):
+            ss.ss_step(h, tk["u"], tk["delta"], x["A"], tk["B"], tk["C"], x["D"], tk["z"],
+                       x["delta_bias"], True, out=ys[i])
 
-    (t,) = _timed_ms([prefill], 10, dev)
-    r = roofline("fwd", kernel_work(2, Dch)["fwd"], E, t, hbm)
-    out["chunked_prefill_bf16_fwd"] = {
-        "workload": f"Bsz={Bsz} Dch={Dch} L={L} N={N} as {P} pieces of {Lp} steps continued "
-                    f"from the carried state (ss_scan_fwd_from_state), bf16 I/O",
-        "gelem_s": round(E / (t * 1e-3) / 1e9, 3), "ms": round(t, 4),
-        **{k: v for k, v in r.items() if k in ("bound", "achieved", "peak", "unit", "frac",
-                                               "resource")}}
-    del x, pieces, ys, h
+    (t,) = _timed_ms([run128], 5, dev, flush=True)
+    units = Bsz * Dch * S
+    out["decode_128_steps"] = {"ms": round(t, 4), "us_per_token": round(1e3 * t / S, 2),
+                               "gelem_s": round(units / t / 1e6, 2),
+                               **_r(roofline(method_work("step", 2, Dch), units, t, peaks))}
+    del x, toks, h, ys
     torch.cuda.empty_cache()
+    if cpu:
+        kinds = {"mamba130m_fwd": ("fwd", 1), "mamba370m_fwd_bwd": ("fwd_bwd", 2),
+                 "long_sequence_fwd": ("fwd", 3), "decode_128_steps": ("decode", 4)}
+        for key, (kind, ci) in kinds.items():
+            c = synth.config(ci)
+            o = oracle_sample(kind, c, c["seed"], target_s=3.0)
+            out[key]["cpu"] = {"gelem_s": o["value"], "cores": o["cores"], "sample": o["short"]}
     return out
 
 
+def next_rows(ss, dev, seed, peaks):
+    """The block's producers of the scan inputs on the bench layer's shape
+    (8 x 1536 x 2048, bf16), L2 flushed before each call: causal conv1d
+    (width 4) + silu forward and backward, and the input projection (x_proj
+    then dt_proj, dt_rank 48, on the tensor cores).  HBM-bound."""
+    import torch
+    cfg = synth.config(CFG_INDEX)
+    Bsz, Dch, L, N, K, R = cfg["Bsz"], cfg["Dch"], cfg["L"], cfg["N"], 4, 48
+    E = Bsz * Dch * L
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed + 7)
+    bf = torch.bfloat16
+    rnd = lambda *s: torch.randn(s, generator=gen, device=dev)
+    x, g = rnd(Bsz, Dch, L).to(bf), rnd(Bsz, Dch, L).to(bf)
+    w, b = rnd(Dch, K) / 2.0, rnd(Dch)
+    u = torch.empty_like(x)
+    grads = {"dx": torch.empty_like(x), "dw": torch.empty((Dch, K), device=dev),
+             "dbias": torch.empty((Dch,), device=dev)}
+    Wx = (rnd(R + 2 * N, Dch) / Dch ** 0.5).to(bf)
+    Wdt = (rnd(Dch, R) / R ** 0.5).to(bf)
+    xo = (torch.empty_like(x), torch.empty((Bsz, N, L), device=dev, dtype=bf),
+          torch.empty((Bsz, N, L), device=dev, dtype=bf))
+    ms = [_timed_ms([f], 16, dev, flush=True)[0] for f in (
+        lambda: ss.ss_conv1d_silu(x, w, b, True, out=u),
+        lambda: ss.ss_conv1d_silu_bwd(x, w, b, True, g, out=grads),
+        lambda: ss.ss_xproj(x, Wx, Wdt, N, out=xo))]
+    nbytes = (2 * 2 * E, 3 * 2 * E,
+              2 * E * 2 + 2 * 2 * Bsz * N * L + 2 * (R + 2 * N) * Dch + 2 * Dch * R)
+    res = {}
+    for name, t, nb in zip(("conv1d_silu_fwd", "conv1d_silu_bwd", "xproj"), ms, nbytes):
+        ach = nb / (t * 1e-3) / 1e9
+        res[name] = {"ms": round(t, 4), "bound": "hbm", "frac": round(ach / peaks.hbm_gbs, 4)}
+    flops = 2 * Bsz * L * Dch * (R + 2 * N) + 2 * Bsz * L * R * Dch
+    res["xproj"]["tensor_tflops"] = round(flops / (ms[2] * 1e-3) / 1e12, 2)
+    res["xproj"]["device_errors"] = ss.ss_check_device_errors()
+    return res
+
+
+# The sources the headline step's kernels are built from: ncu traffic taken
+# on other versions of these files is not reported.
+STEP_SOURCES = ("common.cuh", "launch.h", "scan_fwd.cu", "scan_bwd.cu", "step.cu")
+
+
+def csrc_digest():
+    import hashlib
+    h = hashlib.sha256()
+    for name in STEP_SOURCES:
+        h.update(open(os.path.join(ROOT, "selective_state_space_114_b300", "csrc", name),
+                      "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, when it was
+    taken on the current kernel sources; else None."""
+    try:
+        d = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
+    except Exception:
+        return None
+    if d.get("csrc_digest") != csrc_digest():
+        return None
+    v = d.get("kernels", {}).get(kernel)
+    return None if v is None else v.get("dram_bytes_per_launch")
+
+
 def run_profile_workload(args):
-    """Run a workload's kernels `--profile-iters` times and exit, for an ncu
-    capture of one launch: mamba370m (the fp32 8 x 2048 x 2048 layer, forward
-    then backward) or long_sequence (the bf16 1 x 5120 x 131072 forward; the
-    length may be cut with --profile-L to keep a capture small)."""
+    """Run one workload's kernels --profile-iters times and exit (for an ncu
+    capture): mamba130m (bf16 8 x 1536 x L, fwd + bwd + decode token),
+    mamba370m (fp32 8 x 2048 x L, fwd + bwd), long_sequence (bf16 1 x 5120 x
+    L forward); --profile-L cuts L to keep a capture small."""
     import torch
     import selective_state_space_114_b300 as ss
     dev = torch.device("cuda", 0)
-    ci = {"mamba370m": 2, "long_sequence": 3}[args.profile_workload]
+    ci = {"mamba130m": 1, "mamba370m": 2, "long_sequence": 3}[args.profile_workload]
     cfg = synth.config(ci)
     if args.profile_L:
         cfg = dict(cfg, L=args.profile_L)
-    x, _ = _device_inputs(cfg, dev, cfg["seed"], with_dy=(ci == 2))
+    bwd = ci in (1, 2)
+    x, _ = _device_inputs(cfg, dev, cfg["seed"], with_dy=bwd)
     Bsz, Dch, L, N = cfg["Bsz"], cfg["Dch"], cfg["L"], cfg["N"]
-    args_ = (x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], True)
-    y = torch.empty_like(x["u"])
+    a = (x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], True)
+    y, h = torch.empty_like(x["u"]), torch.empty((Bsz, Dch, N), device=dev)
     ws = None
-    if ci == 2:
-        ws = torch.empty(ss.ss_scan_bwd_workspace_size(Bsz, Dch, L, N, ss.SS_F32), device=dev,
+    if bwd:
+        code = ss.SS_BF16 if cfg["dtype"] == "bf16" else ss.SS_F32
+        ws = torch.empty(ss.ss_scan_bwd_workspace_size(Bsz, Dch, L, N, code), device=dev,
                          dtype=torch.uint8)
     for _ in range(args.profile_iters):
-        ss.ss_scan_fwd(*args_, out=y)
+        ss.ss_scan_fwd(*a, out=y, h_last=h, return_last_state=True)
         if ws is not None:
-            ss.ss_scan_bwd(*args_, x["dy"], workspace=ws)
+            ss.ss_scan_bwd(*a, x["dy"], workspace=ws)
     torch.cuda.synchronize()
     print(json.dumps({"profile_workload": args.profile_workload, "Bsz": Bsz, "Dch": Dch, "L": L,
                       "iters": args.profile_iters}))
@@ -711,6 +699,7 @@ def run_ours(args):
     from selective_state_space_114_b300 import dist as sdist
 
     dev = torch.device("cuda", local)
+    peaks = Peaks(measure_pipes() if rank == 0 else None)
     cfg, conf = workload_config(world)
     seed = sdist.rank_seed(cfg["seed"], rank)
     Bsz, Dch, L, N = cfg["Bsz"], cfg["Dch"], cfg["L"], cfg["N"]
@@ -733,14 +722,10 @@ def run_ours(args):
     bf = torch.bfloat16
     y = torch.empty((Bsz, Dch, L), device=dev, dtype=bf)
     h = torch.empty((Bsz, Dch, N), device=dev, dtype=torch.float32)
-    g = {"du": torch.empty_like(y), "ddelta": torch.empty_like(y), "dz": torch.empty_like(y),
-         "dA": torch.empty((Dch, N), device=dev), "dB": torch.empty((Bsz, N, L), device=dev),
-         "dC": torch.empty((Bsz, N, L), device=dev), "dD": torch.empty((Dch,), device=dev),
-         "ddelta_bias": torch.empty((Dch,), device=dev)}
+    g = _grads(d, dev)
     ws = torch.empty(ss.ss_scan_bwd_workspace_size(Bsz, Dch, L, N, ss.SS_BF16), device=dev,
                      dtype=torch.uint8)
     yt = torch.empty((Bsz, Dch), device=dev, dtype=bf)
-    stages = ("ss_scan_bwd_states", "ss_scan_bwd_reverse", "ss_scan_bwd_reduce")
     names = ["fwd", "bwd_states", "bwd_reverse", "bwd_reduce", "step"]
 
     def one_step(evs=None, src=None):
@@ -754,7 +739,7 @@ def run_ours(args):
         ss.ss_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
                        d["delta_bias"], True, return_last_state=True, out=y, h_last=h)
         rec(1)
-        for i, st in enumerate(stages):
+        for i, st in enumerate(BWD_STAGES):
             ss.ss_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
                            d["delta_bias"], True, d["dy"], workspace=ws, out=g, stages=(st,))
             rec(2 + i)
@@ -784,15 +769,13 @@ def run_ours(args):
     barrier()
     ms_local = start.elapsed_time(end) / K
     ms = sdist.max_over_ranks(ms_local, device=dev)
-    per_kernel = {nm: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K))
-                  for i, nm in enumerate(names)}
+    per = {nm: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K))
+           for i, nm in enumerate(names)}
     value = world * E / (ms * 1e-3) / 1e9
-    fwd_gelem = E / (per_kernel["fwd"] * 1e-3) / 1e9
 
-    decode = decode_step_measure(ss, dev, seed) if rank == 0 else None
-    conv = conv_measure(ss, dev, seed) if rank == 0 else None
-    others = configs_measure(ss, dev, seed) if rank == 0 else None
-    xproj = xproj_measure(ss, dev, seed) if rank == 0 else None
+    configs = config_lines(ss, dev, seed, peaks, cpu=not args.no_cpu_baseline) \
+        if rank == 0 else None
+    nxt = next_rows(ss, dev, seed, peaks) if rank == 0 else None
 
     # end to end through the public API with host buffers
     Ke = max(3, min(K, 10))
@@ -818,36 +801,46 @@ def run_ours(args):
             dist.destroy_process_group()
         return 0
 
-    hbm, peak_src = load_peaks()
-    work = kernel_work(2, Dch)
-    roofs = {nm: roofline(nm, work[nm], E, per_kernel[nm], hbm, ncu_traffic(nm))
-             for nm in names if nm in work}
-    dominant = max(roofs, key=lambda nm: per_kernel[nm])
+    work = {"fwd": method_work("fwd", 2, Dch), "bwd_reverse": method_work("bwd", 2, Dch)}
+    kernels = {}
+    for nm in names:
+        kernels[nm] = {"ms": round(per[nm], 4), "share": round(per[nm] / sum(per.values()), 4)}
+        if nm in work:
+            r = roofline(work[nm], E, per[nm], peaks)
+            kernels[nm].update(frac=r["frac"], bound=r.get("resource", r["bound"]))
+    rstep = roofline(method_work("step", 2, Dch), Bsz * Dch, per["step"], peaks)
+    kernels["step"].update(frac=rstep["frac"], bound="hbm")
+    tb = per["bwd_states"] + per["bwd_reverse"] + per["bwd_reduce"]
+    rbwd = roofline(method_work("bwd", 2, Dch), E, tb, peaks)
+    dominant = max(("fwd", "bwd_reverse"), key=lambda nm: per[nm])
+    top = roofline(work[dominant], E, per[dominant], peaks, ncu_traffic(dominant))
+    top.pop("bound_ms", None)
+    # the standard keys first; the per-kernel and per-workload detail last
+    # (a reader of the line's tail sees it)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": conf,
-        "fwd_gelem_s": round(fwd_gelem, 3),
-        "roofline": roofs[dominant],
-        "roofline_peak_source": f"fp32: {SMS} SMs x {FP32_LANES} ops/clk x {SM_MAX_MHZ} MHz; "
-                                f"mufu: {SMS} SMs x {MUFU_LANES} ops/clk (measured) x "
-                                f"{SM_MAX_MHZ} MHz; hbm: {hbm} GB/s of {peak_src}",
-        "kernels": {nm: {"ms": round(per_kernel[nm], 4),
-                         "share": round(per_kernel[nm] / sum(per_kernel.values()), 4),
-                         **({"frac": roofs[nm]["frac"], "bound": roofs[nm]["bound"]}
-                            if nm in roofs else {})} for nm in names},
         "gpu_launches": K * LAUNCHES_PER_STEP,
-        "decode_step": decode,
-        "conv1d_silu": conv,
-        "other_workloads": others,
-        "xproj": xproj,
         "e2e": {"value": round(world * E / (e2e_ms * 1e-3) / 1e9, 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 3)},
         "clocks": clk.summary(),
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg, seed)
+        cb = oracle_sample("step", cfg, seed, target_s=12.0)
+        cb.pop("short")
+        line["cpu_baseline"] = cb
+    pk = peaks.describe()
+    pk.pop("per_sm_clk")
+    line.update({
+        "peaks": pk,
+        "next_rows": nxt,
+        "roofline": {"kernel": dominant, **top},
+        "configs": configs,
+        "backward": {"ms": round(tb, 4), "frac": rbwd["frac"], "bound": rbwd.get("resource")},
+        "kernels": kernels,
+    })
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -861,12 +854,22 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true",
-                    help="skip the oracle timing on the host cores")
-    ap.add_argument("--profile-workload", choices=["mamba370m", "long_sequence"],
+                    help="skip the oracle timings on the host cores")
+    ap.add_argument("--pipes", action="store_true",
+                    help="print the pipe microbenchmark's per-SM rates and exit")
+    ap.add_argument("--profile-workload", choices=["mamba130m", "mamba370m", "long_sequence"],
                     help="only run that workload's kernels (for an ncu capture) and exit")
     ap.add_argument("--profile-L", type=int, default=0)
     ap.add_argument("--profile-iters", type=int, default=2)
     args = ap.parse_args()
+    if args.pipes:
+        import torch
+        torch.cuda.set_device(0)
+        rates = measure_pipes()
+        smem = measure_pipes(tests=SMEM_TESTS)
+        print(json.dumps({"per_sm_per_clock": rates, "smem_clocks_per_access": smem,
+                          "peaks": Peaks(rates).describe(), "gpu": torch.cuda.get_device_name(0)}))
+        return 0 if rates else 1
     if args.profile_workload:
         return run_profile_workload(args)
     if args.impl == "reference":
