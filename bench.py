@@ -654,12 +654,16 @@ def ncu_traffic(kernel):
 
 def run_profile_workload(args):
     """Run one workload's kernels --profile-iters times and exit (for an ncu
-    capture): mamba130m (bf16 8 x 1536 x L, fwd + bwd + decode token),
-    mamba370m (fp32 8 x 2048 x L, fwd + bwd), long_sequence (bf16 1 x 5120 x
-    L forward); --profile-L cuts L to keep a capture small."""
+    capture): mamba130m (bf16 8 x 1536 x L, fwd + bwd), mamba370m (fp32 8 x
+    2048 x L, fwd + bwd), long_sequence (bf16 1 x 5120 x L forward), decode
+    (one token on 256 x 5120), producers (conv1d + silu fwd and bwd and the
+    input projection on bf16 8 x 1536 x L); --profile-L cuts L to keep a
+    capture small."""
     import torch
     import selective_state_space_114_b300 as ss
     dev = torch.device("cuda", 0)
+    if args.profile_workload in ("decode", "producers"):
+        return _profile_other(args, ss, dev)
     ci = {"mamba130m": 1, "mamba370m": 2, "long_sequence": 3}[args.profile_workload]
     cfg = synth.config(ci)
     if args.profile_L:
@@ -680,6 +684,42 @@ def run_profile_workload(args):
             ss.ss_scan_bwd(*a, x["dy"], workspace=ws)
     torch.cuda.synchronize()
     print(json.dumps({"profile_workload": args.profile_workload, "Bsz": Bsz, "Dch": Dch, "L": L,
+                      "iters": args.profile_iters}))
+    return 0
+
+
+def _profile_other(args, ss, dev):
+    import torch
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5)
+    bf = torch.bfloat16
+    rnd = lambda *s: torch.randn(s, generator=gen, device=dev)
+    if args.profile_workload == "decode":
+        cfg = synth.config(4)
+        Bsz, Dch, N = cfg["Bsz"], cfg["Dch"], cfg["N"]
+        x, _ = _device_inputs(dict(cfg, L=1), dev, cfg["seed"])
+        tk = {k: rnd(*shp).to(bf) for k, shp in (("u", (Bsz, Dch)), ("delta", (Bsz, Dch)),
+                                                ("z", (Bsz, Dch)), ("B", (Bsz, N)),
+                                                ("C", (Bsz, N)))}
+        h = torch.zeros((Bsz, Dch, N), device=dev)
+        for _ in range(args.profile_iters):
+            ss.ss_step(h, tk["u"], tk["delta"], x["A"], tk["B"], tk["C"], x["D"], tk["z"],
+                       x["delta_bias"], True)
+        shape = {"Bsz": Bsz, "Dch": Dch}
+    else:
+        cfg = synth.config(CFG_INDEX)
+        Bsz, Dch, L, N, K, R = (cfg["Bsz"], cfg["Dch"], args.profile_L or cfg["L"], cfg["N"],
+                                4, 48)
+        x, g = rnd(Bsz, Dch, L).to(bf), rnd(Bsz, Dch, L).to(bf)
+        w, b = rnd(Dch, K) / 2.0, rnd(Dch)
+        Wx, Wdt = (rnd(R + 2 * N, Dch) / Dch ** 0.5).to(bf), (rnd(Dch, R) / R ** 0.5).to(bf)
+        for _ in range(args.profile_iters):
+            ss.ss_conv1d_silu(x, w, b, True)
+            ss.ss_conv1d_silu_bwd(x, w, b, True, g)
+            ss.ss_xproj(x, Wx, Wdt, N)
+        shape = {"Bsz": Bsz, "Dch": Dch, "L": L}
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_workload": args.profile_workload, **shape,
                       "iters": args.profile_iters}))
     return 0
 
@@ -773,9 +813,9 @@ def run_ours(args):
            for i, nm in enumerate(names)}
     value = world * E / (ms * 1e-3) / 1e9
 
-    configs = config_lines(ss, dev, seed, peaks, cpu=not args.no_cpu_baseline) \
-        if rank == 0 else None
-    nxt = next_rows(ss, dev, seed, peaks) if rank == 0 else None
+    side = rank == 0 and not args.step_only
+    configs = config_lines(ss, dev, seed, peaks, cpu=not args.no_cpu_baseline) if side else None
+    nxt = next_rows(ss, dev, seed, peaks) if side else None
 
     # end to end through the public API with host buffers
     Ke = max(3, min(K, 10))
@@ -855,9 +895,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timings on the host cores")
+    ap.add_argument("--step-only", action="store_true",
+                    help="time the headline step only (no per-workload or producer entries)")
     ap.add_argument("--pipes", action="store_true",
                     help="print the pipe microbenchmark's per-SM rates and exit")
-    ap.add_argument("--profile-workload", choices=["mamba130m", "mamba370m", "long_sequence"],
+    ap.add_argument("--profile-workload",
+                    choices=["mamba130m", "mamba370m", "long_sequence", "decode", "producers"],
                     help="only run that workload's kernels (for an ncu capture) and exit")
     ap.add_argument("--profile-L", type=int, default=0)
     ap.add_argument("--profile-iters", type=int, default=2)
