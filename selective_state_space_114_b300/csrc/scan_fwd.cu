@@ -319,14 +319,23 @@ struct FwdRowsCfg {
   static constexpr int RAWB = T * (int)sizeof(E) + 16;  // raw B/C row bytes (padded)
   static constexpr int CF_OFF = NS * T + 16;     // C tile offset from B tile (floats)
   static constexpr int DDS = 2 * T + 4;          // (dt, dt*u) row stride (floats)
-  static constexpr int YPS = 4 * T + 16;         // partial row stride (floats)
+  static constexpr int YPS = 4 * T;              // partial row stride (floats, 128-byte rows)
   static constexpr size_t raw_bytes = 2ull * 2 * NS * RAWB;
   static constexpr size_t smem =
       raw_bytes + sizeof(float) * ((size_t)CF_OFF + NS * T + (size_t)R * DDS + (size_t)R * YPS);
   static_assert(NV >= 1 && R * VPR == NV * NT, "whole vectors per thread");
-  static_assert(T % 4 == 0 && (RAWB % 16) == 0 && R % (8 * NR) == 0, "tile shape");
+  static_assert(T % 8 == 0 && (RAWB % 16) == 0 && R % (8 * NR) == 0, "tile shape");
   static_assert(NS % 8 == 0 && NS <= 64, "state pairs per lane");
 };
+
+// Position of 16-byte chunk c (the partials of steps 4 (c / 4) .. + 3 from
+// state group c % 4) in partial row r.  Within each 128-byte line the chunks
+// are permuted by row so that both access patterns are conflict-free: phase B
+// (eight consecutive rows, one chunk) and phase C (two consecutive rows, the
+// four chunks of a step group rotated by the reading lane).
+__device__ __forceinline__ int ypos(int r, int c) {
+  return (c & ~7) | ((((c & 7) + 4 * (r & 1)) & 7) ^ ((r >> 1) & 3));
+}
 
 // SPL consecutive floats of shared memory (16-byte aligned when SPL % 4 == 0,
 // else 8-byte aligned) as SPL / 2 float2.
@@ -366,8 +375,13 @@ __global__ void __launch_bounds__(4 * R / NR)
   const E* Bb = static_cast<const E*>(p.B) + b * NS * L;
   const E* Cb = static_cast<const E*>(p.C) + b * NS * L;
 
-  // recurrence lane: rows qr + j R / NR (j < NR), states SPL qk .. SPL qk + SPL - 1
-  const int qr = tid >> 2, qk = tid & 3;
+  // recurrence lane: rows qr + j R / NR (j < NR), states SPL qk .. SPL qk + SPL - 1.
+  // The four lanes of a row sit one per quarter-warp (lanes l, l + 8, l + 16,
+  // l + 24 of a warp), so that each quarter-warp reads a single address of the
+  // B / C tile: a 128-bit load then takes two shared-memory wavefronts, where
+  // four lanes per row side by side (the same address in every quarter-warp)
+  // take four.
+  const int qr = (tid >> 5) * 8 + (tid & 7), qk = (tid >> 3) & 3;
   float2 A2[NR][SPL / 2], h[NR][SPL / 2];
 #pragma unroll
   for (int j = 0; j < NR; ++j) {
@@ -457,7 +471,7 @@ __global__ void __launch_bounds__(4 * R / NR)
           float2 lo = make_float2(0.f, 0.f), hi = lo;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const float4 q = prow[4 * g + ((kk + rot) & 3)];
+            const float4 q = prow[ypos(er[m], 4 * g + ((kk + rot) & 3))];
             lo = add2(lo, make_float2(q.x, q.y));
             hi = add2(hi, make_float2(q.z, q.w));
           }
@@ -582,7 +596,7 @@ __global__ void __launch_bounds__(4 * R / NR)
         }
 #pragma unroll
         for (int j = 0; j < NR; ++j)
-          reinterpret_cast<float4*>(yp + (qr + j * (R / NR)) * Cfg::YPS)[4 * g + qk] =
+          reinterpret_cast<float4*>(yp + (qr + j * (R / NR)) * Cfg::YPS)[ypos(qr + j * (R / NR), 4 * g + qk)] =
               make_float4(yv[j][0], yv[j][1], yv[j][2], yv[j][3]);
       }
     }

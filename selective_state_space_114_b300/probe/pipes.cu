@@ -152,12 +152,12 @@ __global__ void __launch_bounds__(1024) smem_kernel(int iters, long long* cyc, u
           asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                        : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
                        : "r"(b + k * 1024));
-          acc += v0;
+          acc += (v0 ^ v1) + (v2 ^ v3);  // every word live: the load stays 128-bit
         }
       } else if (bytes == 8) {
         unsigned v0, v1;
         asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v0), "=r"(v1) : "r"(b + k * 1024));
-        acc += v0;
+        acc += v0 ^ v1;
       } else {
         unsigned v0;
         asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v0) : "r"(b + k * 1024));
