@@ -801,6 +801,10 @@ def run_ours(args):
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        # the GPU spins first (about 12 ms + 1.2 ms per step) so that the host
+        # has enqueued the timed steps before the first one runs: the events
+        # then see device time only, not the host's launch rate
+        torch.cuda._sleep(25_000_000 + 2_500_000 * K)
         start.record()
         for k in range(K):
             one_step(evs[k])
