@@ -7,6 +7,9 @@
 // each updating N / 4 states (with N = 16 one 16-byte load and store, so a
 // warp moves 512 contiguous bytes of h per access); the C.h sum is finished
 // with two shuffles inside the group of four.
+// Successive steps overlap (programmatic dependent launch): a step lets the
+// next one start at once; the next loads its token, A, D and delta_bias, then
+// waits for the previous grid to complete before it reads or writes h and y.
 #include "common.cuh"
 #include "launch.h"
 
@@ -67,16 +70,22 @@ __global__ void __launch_bounds__(kStepThreads) step_kernel(StepArgs p) {
   const int64_t dd = valid ? d : 0;
   const int64_t rr = b * p.Dch + dd;
 
-  // every load first (rows past Dch read row 0 of the batch and store nothing)
+  // the next step may be scheduled now; it waits below for this grid to end
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // every load first (rows past Dch read row 0 of the batch and store nothing);
+  // the token's inputs before the wait, the state after it
   float Bv[SPL], Cv[SPL], hv[SPL], Av[SPL];
   load_spl<Io, SPL>(static_cast<const T*>(p.B) + b * NS + SPL * q, Bv);
   load_spl<Io, SPL>(static_cast<const T*>(p.C) + b * NS + SPL * q, Cv);
-  load_spl<IoF32, SPL>(p.h + rr * NS + SPL * q, hv);
   load_spl<IoF32, SPL>(p.A + dd * NS + SPL * q, Av);
   const float uu = Io::to_f(static_cast<const T*>(p.u)[rr]);
   const float x = Io::to_f(static_cast<const T*>(p.delta)[rr]) +
                   (p.delta_bias ? p.delta_bias[dd] : 0.f);
   const float zz = p.z ? Io::to_f(static_cast<const T*>(p.z)[rr]) : 0.f;
+  const float Dd = (valid && p.D) ? p.D[d] : 0.f;
+  // the previous kernel of the stream has completed and its writes are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  load_spl<IoF32, SPL>(p.h + rr * NS + SPL * q, hv);
 
   const float dt = p.softplus ? softplus_fast(x) : x;
   const float dtu = dt * uu;
@@ -100,22 +109,39 @@ __global__ void __launch_bounds__(kStepThreads) step_kernel(StepArgs p) {
   yp += __shfl_xor_sync(0xffffffffu, yp, 1);
   yp += __shfl_xor_sync(0xffffffffu, yp, 2);
   if (valid && q == 0) {
-    float y = fmaf(p.D ? p.D[d] : 0.f, uu, yp);
+    float y = fmaf(Dd, uu, yp);
     if (p.z) y *= zz * sigmoid_f(zz);
     static_cast<T*>(p.y)[rr] = Io::from_f(y);
   }
 }
 
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel of the stream runs, and waits for it (griddepcontrol)
+// before it touches the state.
+template <typename Io, int NS>
+cudaError_t launch_step_ns(const StepArgs& a, const dim3& grid, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kStepThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, step_kernel<Io, NS>, a);
+}
+
 template <typename Io>
 cudaError_t launch_step_t(const StepArgs& a, const dim3& grid, cudaStream_t s) {
   switch (a.N) {
-    case 8: step_kernel<Io, 8><<<grid, kStepThreads, 0, s>>>(a); break;
-    case 16: step_kernel<Io, 16><<<grid, kStepThreads, 0, s>>>(a); break;
-    case 32: step_kernel<Io, 32><<<grid, kStepThreads, 0, s>>>(a); break;
-    case 64: step_kernel<Io, 64><<<grid, kStepThreads, 0, s>>>(a); break;
+    case 8: return launch_step_ns<Io, 8>(a, grid, s);
+    case 16: return launch_step_ns<Io, 16>(a, grid, s);
+    case 32: return launch_step_ns<Io, 32>(a, grid, s);
+    case 64: return launch_step_ns<Io, 64>(a, grid, s);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace
