@@ -768,26 +768,25 @@ def run_ours(args):
     yt = torch.empty((Bsz, Dch), device=dev, dtype=bf)
     names = ["fwd", "bwd_states", "bwd_reverse", "bwd_reduce", "step"]
 
-    def one_step(evs=None, src=None):
-        if src is not None:  # e2e: this step's inputs arrive from pinned host memory
-            for k, v in src[0].items():
-                d[k].copy_(v, non_blocking=True)
-            for k, v in src[1].items():
-                dt[k].copy_(v, non_blocking=True)
+    def one_step(evs=None, bufs=None):
+        """One pass of the path on the current stream; bufs = (inputs, token,
+        outputs, state) of an end-to-end buffer set, else the resident ones."""
+        dd, tk, out, hh = bufs if bufs is not None else (d, dt, dict(y=y, yt=yt, **g), h)
+        gg = {k: out[k] for k in g}
         rec = (lambda i: evs[i].record()) if evs is not None else (lambda i: None)
         rec(0)
-        ss.ss_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
-                       d["delta_bias"], True, return_last_state=True, out=y, h_last=h)
+        ss.ss_scan_fwd(dd["u"], dd["delta"], dd["A"], dd["B"], dd["C"], dd["D"], dd["z"],
+                       dd["delta_bias"], True, return_last_state=True, out=out["y"], h_last=hh)
         rec(1)
         for i, st in enumerate(BWD_STAGES):
-            ss.ss_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
-                           d["delta_bias"], True, d["dy"], workspace=ws, out=g, stages=(st,))
+            ss.ss_scan_bwd(dd["u"], dd["delta"], dd["A"], dd["B"], dd["C"], dd["D"], dd["z"],
+                           dd["delta_bias"], True, dd["dy"], workspace=ws, out=gg, stages=(st,))
             rec(2 + i)
-        ss.ss_step(h, dt["u"], dt["delta"], d["A"], dt["B"], dt["C"], d["D"], dt["z"],
-                   d["delta_bias"], True, out=yt)
+        ss.ss_step(hh, tk["u"], tk["delta"], dd["A"], tk["B"], tk["C"], dd["D"], tk["z"],
+                   dd["delta_bias"], True, out=out["yt"])
         rec(5)
         if world > 1:
-            sdist.allreduce_param_grads(g)
+            sdist.allreduce_param_grads(gg)
 
     def barrier():
         if world > 1:
@@ -821,24 +820,57 @@ def run_ours(args):
     configs = config_lines(ss, dev, seed, peaks, cpu=not args.no_cpu_baseline) if side else None
     nxt = next_rows(ss, dev, seed, peaks) if side else None
 
-    # end to end through the public API with host buffers
-    Ke = max(3, min(K, 10))
+    # end to end through the public API with host buffers: every step copies
+    # its inputs in from pinned host memory and its outputs back out.  The
+    # steps are pipelined over three streams (copy in, compute, copy out) with
+    # two buffer sets, so the copies of one step overlap the kernels of
+    # another and the two copy directions overlap each other.
+    Ke = max(4, min(K, 10))
     outs = {"y": y, "yt": yt, **g}
-    hout = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+    sets = [({k: torch.empty_like(v) for k, v in d.items()},
+             {k: torch.empty_like(v) for k, v in dt.items()},
+             {k: torch.empty_like(v) for k, v in outs.items()},
+             torch.empty_like(h)) for _ in range(2)]
+    hout = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+            for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in list(hx.values()) + list(ht.values()))
     d2h = sum(v.numel() * v.element_size() for v in outs.values())
+    s_comp = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    in_done, comp_done, out_done = ([ev() for _ in range(Ke)] for _ in range(3))
     barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(Ke):
-        one_step(src=(hx, ht))
-        for k, v in outs.items():
-            hout[k].copy_(v, non_blocking=True)
-    e1.record()
+    e0.record(s_comp)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    for k in range(Ke):
+        dd, tk, out, hh = sets[k % 2]
+        with torch.cuda.stream(s_in):
+            if k >= 2:
+                s_in.wait_event(comp_done[k - 2])  # the set's inputs are free again
+            for n, v in hx.items():
+                dd[n].copy_(v, non_blocking=True)
+            for n, v in ht.items():
+                tk[n].copy_(v, non_blocking=True)
+            in_done[k].record(s_in)
+        s_comp.wait_event(in_done[k])
+        if k >= 2:
+            s_comp.wait_event(out_done[k - 2])  # the set's outputs have been read out
+        one_step(bufs=(dd, tk, out, hh))
+        comp_done[k].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[k])
+            for n, v in out.items():
+                hout[k % 2][n].copy_(v, non_blocking=True)
+            out_done[k].record(s_out)
+    s_comp.wait_event(out_done[Ke - 1])
+    e1.record(s_comp)
     torch.cuda.synchronize()
     barrier()
     e2e_ms = sdist.max_over_ranks(e0.elapsed_time(e1) / Ke, device=dev)
+    del sets
 
     if rank != 0:
         if world > 1:

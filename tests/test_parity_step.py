@@ -107,3 +107,32 @@ def test_config4_128_steps_state_checked_every_step():
         check(to_host64(hs), href, "f32", f"config4 step {k} h")
         check(to_host64(ys), yref, "bf16", f"config4 step {k} y")
     assert torch.isfinite(h).all()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_steps_back_to_back_without_sync(dtype):
+    """Successive steps overlap on the device (each is scheduled while the
+    previous runs and waits for it before touching h): 64 steps enqueued with
+    no host synchronisation, every token's y kept, then all of them and the
+    final state checked against the oracle.  A GPU spin first lets the host
+    enqueue every step before the first one runs."""
+    Bsz, Dch, steps = 16, 1024, 64
+    cfg, A, D, bias = _params(dtype, Bsz, Dch, 404)
+    h = torch.zeros((Bsz, Dch, 16), device="cuda")
+    Ad, Dd, bd = (torch.from_numpy(np.array(v)).cuda() for v in (A, D, bias))
+    toks = [synth.step_inputs(cfg, k) for k in range(steps)]
+    dev_toks = [{n: to_dev(v, dtype) for n, v in s.items()} for s in toks]
+    ys = [torch.empty((Bsz, Dch), device="cuda", dtype=torch.float32 if dtype == "f32"
+                      else torch.bfloat16) for _ in range(steps)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(20_000_000)
+    for k in range(steps):
+        sd = dev_toks[k]
+        ss.ss_step(h, sd["u"], sd["delta"], Ad, sd["B"], sd["C"], Dd, sd["z"], bd, True, out=ys[k])
+    torch.cuda.synchronize()
+    href = np.zeros((Bsz, Dch, 16))
+    for k in range(steps):
+        w = {n: synth.widen(v) for n, v in toks[k].items()}
+        yref, href = oracle.step(href, w["u"], w["delta"], A, w["B"], w["C"], D, w["z"], bias, True)
+        check(to_host64(ys[k]), yref, out_kind(dtype), f"back-to-back step {k} y")
+    check(to_host64(h), href, "f32", "back-to-back final h")
