@@ -627,13 +627,17 @@ def next_rows(ss, dev, seed, peaks):
 
 # The sources the headline step's kernels are built from: ncu traffic taken
 # on other versions of these files is not reported.
-STEP_SOURCES = ("common.cuh", "launch.h", "scan_fwd.cu", "scan_bwd.cu", "step.cu")
+# the sources each timed kernel is built from (its ncu figures hold while they
+# are unchanged)
+KERNEL_SOURCES = {"fwd": ("common.cuh", "launch.h", "scan_fwd.cu"),
+                  "bwd_states": ("common.cuh", "launch.h", "scan_bwd.cu"),
+                  "bwd_reverse": ("common.cuh", "launch.h", "scan_bwd.cu")}
 
 
-def csrc_digest():
+def csrc_digest(kernel):
     import hashlib
     h = hashlib.sha256()
-    for name in STEP_SOURCES:
+    for name in KERNEL_SOURCES[kernel]:
         h.update(open(os.path.join(ROOT, "selective_state_space_114_b300", "csrc", name),
                       "rb").read())
     return h.hexdigest()[:16]
@@ -646,10 +650,10 @@ def ncu_traffic(kernel):
         d = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
     except Exception:
         return None
-    if d.get("csrc_digest") != csrc_digest():
-        return None
     v = d.get("kernels", {}).get(kernel)
-    return None if v is None else v.get("dram_bytes_per_launch")
+    if v is None or kernel not in KERNEL_SOURCES or v.get("csrc_digest") != csrc_digest(kernel):
+        return None
+    return v.get("dram_bytes_per_launch")
 
 
 def run_profile_workload(args):
