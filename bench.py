@@ -4,9 +4,11 @@ path, with the roofline of every kernel and the fp64 oracle timed beside it.
 
 Headline step (the JSON line's ``value``): one pass of the whole path over the
 Mamba-130M-shaped layer (Bsz=8, Dch=1536, L=2048, N=16, bf16 I/O, float32
-state): ss_scan_fwd + ss_scan_bwd (its three stages) + one ss_step decode
-token continuing from the forward's final state (+ for N > 1 replicas the
-all-reduce of dA, dD, ddelta_bias).  Synthetic seeded data with the
+state): the forward, keeping the chunk states for the backward
+(ss_scan_fwd_save) + its backward (ss_scan_bwd_saved's three stages) + one
+ss_step decode token continuing from the forward's final state (+ for N > 1
+replicas the all-reduce of dA, dD, ddelta_bias).  The backward that
+recomputes the chunk states (ss_scan_bwd) is timed beside it.  Synthetic seeded data with the
 workload's distributions (u, z, B, C, delta_raw, dy ~ N(0,1); A[d,n] =
 -(n+1); D ~ N(0,1); delta_bias = inverse softplus of dt, dt log-uniform in
 [1e-3, 1e-1]).
@@ -521,8 +523,9 @@ def config_lines(ss, dev, seed, peaks, cpu=True):
     y, g = torch.empty_like(x["u"]), _grads(x, dev)
     ws = torch.empty(ss.ss_scan_bwd_workspace_size(Bsz, Dch, L, N, ss.SS_F32), device=dev,
                      dtype=torch.uint8)
-    fns = [lambda: ss.ss_scan_fwd(*args, out=y)] + [
-        lambda st=st: ss.ss_scan_bwd(*args, x["dy"], workspace=ws, out=g, stages=(st,))
+    fns = [lambda: ss.ss_scan_fwd(*args, out=y, save_to=ws)] + [
+        lambda st=st: ss.ss_scan_bwd(*args, x["dy"], workspace=ws, out=g, stages=(st,),
+                                     saved=True)
         for st in BWD_STAGES]
     ms = _timed_ms(fns, 10, dev)
     tb = sum(ms[1:])
@@ -683,9 +686,9 @@ def run_profile_workload(args):
         ws = torch.empty(ss.ss_scan_bwd_workspace_size(Bsz, Dch, L, N, code), device=dev,
                          dtype=torch.uint8)
     for _ in range(args.profile_iters):
-        ss.ss_scan_fwd(*a, out=y, h_last=h, return_last_state=True)
+        ss.ss_scan_fwd(*a, out=y, h_last=h, return_last_state=True, save_to=ws)
         if ws is not None:
-            ss.ss_scan_bwd(*a, x["dy"], workspace=ws)
+            ss.ss_scan_bwd(*a, x["dy"], workspace=ws, saved=True)
     torch.cuda.synchronize()
     print(json.dumps({"profile_workload": args.profile_workload, "Bsz": Bsz, "Dch": Dch, "L": L,
                       "iters": args.profile_iters}))
@@ -780,11 +783,13 @@ def run_ours(args):
         rec = (lambda i: evs[i].record()) if evs is not None else (lambda i: None)
         rec(0)
         ss.ss_scan_fwd(dd["u"], dd["delta"], dd["A"], dd["B"], dd["C"], dd["D"], dd["z"],
-                       dd["delta_bias"], True, return_last_state=True, out=out["y"], h_last=hh)
+                       dd["delta_bias"], True, return_last_state=True, out=out["y"], h_last=hh,
+                       save_to=ws)
         rec(1)
         for i, st in enumerate(BWD_STAGES):
             ss.ss_scan_bwd(dd["u"], dd["delta"], dd["A"], dd["B"], dd["C"], dd["D"], dd["z"],
-                           dd["delta_bias"], True, dd["dy"], workspace=ws, out=gg, stages=(st,))
+                           dd["delta_bias"], True, dd["dy"], workspace=ws, out=gg, stages=(st,),
+                           saved=True)
             rec(2 + i)
         ss.ss_step(hh, tk["u"], tk["delta"], dd["A"], tk["B"], tk["C"], dd["D"], tk["z"],
                    dd["delta_bias"], True, out=out["yt"])
@@ -821,6 +826,12 @@ def run_ours(args):
     value = world * E / (ms * 1e-3) / 1e9
 
     side = rank == 0 and not args.step_only
+    # the first backward stage when the chunk states are recomputed (the
+    # backward without a saving forward): summaries and carries of both
+    (t_states_recomputed,) = _timed_ms(
+        [lambda: ss.ss_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                                d["delta_bias"], True, d["dy"], workspace=ws, out=g,
+                                stages=("ss_scan_bwd_states",))], 10, dev) if side else (None,)
     configs = config_lines(ss, dev, seed, peaks, cpu=not args.no_cpu_baseline) if side else None
     nxt = next_rows(ss, dev, seed, peaks) if side else None
 
@@ -918,7 +929,9 @@ def run_ours(args):
         "next_rows": nxt,
         "roofline": {"kernel": dominant, **top},
         "configs": configs,
-        "backward": {"ms": round(tb, 4), "frac": rbwd["frac"], "bound": rbwd.get("resource")},
+        "backward": {"ms": round(tb, 4), "frac": rbwd["frac"], "bound": rbwd.get("resource"),
+                     "states_stage_when_recomputed_ms": (round(t_states_recomputed, 4)
+                                                         if t_states_recomputed else None)},
         "kernels": kernels,
     })
     print(json.dumps(line), flush=True)

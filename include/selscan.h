@@ -205,6 +205,54 @@ ss_status ss_scan_bwd_reduce(const void* u, const void* delta, const float* A, c
                              ss_stream_t stream);
 
 /*
+ * Forward and backward with the chunk states kept in between (a training
+ * step's forward followed by its backward on the same inputs).  The
+ * backward above recomputes, in its first stage, the state entering each
+ * 128-step chunk; the row-sequential forward kernel passes through those
+ * states anyway.  ss_scan_fwd_save is ss_scan_fwd that also writes them into
+ * a backward workspace (0.5 bytes of state per scanned element at N = 16:
+ * the states at chunk boundaries, not the per-step states, which the
+ * backward still recomputes).  ss_scan_bwd_saved is ss_scan_bwd for a
+ * workspace so prepared: its first stage computes only the adjoint carries.
+ *   ss_scan_fwd_save : ss_scan_fwd's arguments plus workspace and
+ *                      workspace_bytes (device, 16-byte aligned, at least
+ *                      ss_scan_bwd_workspace_size for the same sizes;
+ *                      SS_ERR_WORKSPACE otherwise).  Shapes whose forward
+ *                      runs the chunked kernels (few rows) get the chunk
+ *                      states from the backward's state summaries, run
+ *                      after the forward on the same stream.
+ *   ss_scan_bwd_saved : ss_scan_bwd's arguments; the workspace must hold the
+ *                      chunk states ss_scan_fwd_save wrote for the same u,
+ *                      delta, A, B, delta_bias, softplus and sizes, with no
+ *                      other use of that workspace in between (otherwise
+ *                      the gradients are wrong; nothing detects it).
+ *   ss_scan_bwd_states_saved : ss_scan_bwd_saved's first stage (then
+ *                      ss_scan_bwd_reverse and ss_scan_bwd_reduce, as for
+ *                      ss_scan_bwd_states).
+ * Results equal ss_scan_fwd / ss_scan_bwd up to rounding: the chunk states
+ * come from the forward's recurrence instead of the backward's summaries.
+ */
+ss_status ss_scan_fwd_save(const void* u, const void* delta, const float* A, const void* B,
+                           const void* C, const float* D, const void* z,
+                           const float* delta_bias, int softplus, int64_t Bsz, int64_t Dch,
+                           int64_t L, int64_t N, ss_dtype dtype, void* y, float* h_last,
+                           void* workspace, size_t workspace_bytes, ss_stream_t stream);
+ss_status ss_scan_bwd_saved(const void* u, const void* delta, const float* A, const void* B,
+                            const void* C, const float* D, const void* z,
+                            const float* delta_bias, int softplus, const void* dy, int64_t Bsz,
+                            int64_t Dch, int64_t L, int64_t N, ss_dtype dtype, void* du,
+                            void* ddelta, float* dA, float* dB, float* dC, float* dD, void* dz,
+                            float* ddelta_bias, void* workspace, size_t workspace_bytes,
+                            ss_stream_t stream);
+ss_status ss_scan_bwd_states_saved(const void* u, const void* delta, const float* A,
+                                   const void* B, const void* C, const float* D, const void* z,
+                                   const float* delta_bias, int softplus, const void* dy,
+                                   int64_t Bsz, int64_t Dch, int64_t L, int64_t N,
+                                   ss_dtype dtype, void* du, void* ddelta, float* dA, float* dB,
+                                   float* dC, float* dD, void* dz, float* ddelta_bias,
+                                   void* workspace, size_t workspace_bytes, ss_stream_t stream);
+
+/*
  * One recurrent step (the "RNN form" used for token-by-token decoding;
  * "mamba.py" page, step function; "Mamba 7.9.1", section 6.2):
  *   in/out: h [Bsz][Dch][N] float32, updated in place;

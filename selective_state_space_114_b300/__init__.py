@@ -59,12 +59,15 @@ def _load() -> ctypes.CDLL:
     lib.ss_scan_fwd.restype = ci
     lib.ss_scan_fwd_from_state.argtypes = [p] * 8 + [ci, p, i64, i64, i64, i64, ci, p, p, p]
     lib.ss_scan_fwd_from_state.restype = ci
+    lib.ss_scan_fwd_save.argtypes = [p] * 8 + [ci, i64, i64, i64, i64, ci, p, p, p, sz, p]
+    lib.ss_scan_fwd_save.restype = ci
     lib.ss_scan_bwd_workspace_size.argtypes = [i64, i64, i64, i64, ci, ctypes.POINTER(sz)]
     lib.ss_scan_bwd_workspace_size.restype = ci
     lib.ss_scan_bwd.argtypes = ([p] * 8 + [ci, p, i64, i64, i64, i64, ci] + [p] * 8 +
                                 [p, sz, p])
     lib.ss_scan_bwd.restype = ci
-    for name in ("ss_scan_bwd_states", "ss_scan_bwd_reverse", "ss_scan_bwd_reduce"):
+    for name in ("ss_scan_bwd_states", "ss_scan_bwd_reverse", "ss_scan_bwd_reduce",
+                 "ss_scan_bwd_saved", "ss_scan_bwd_states_saved"):
         f = getattr(lib, name)
         f.argtypes = lib.ss_scan_bwd.argtypes
         f.restype = ci
@@ -91,9 +94,9 @@ def _load() -> ctypes.CDLL:
 
 _lib = _load()
 EXPORTED_SYMBOLS = ("ss_status_str", "ss_version", "ss_scan_fwd", "ss_scan_fwd_from_state",
-                    "ss_scan_bwd_workspace_size",
+                    "ss_scan_fwd_save", "ss_scan_bwd_workspace_size",
                     "ss_scan_bwd", "ss_scan_bwd_states", "ss_scan_bwd_reverse",
-                    "ss_scan_bwd_reduce", "ss_step", "ss_conv1d_silu_fwd",
+                    "ss_scan_bwd_reduce", "ss_scan_bwd_saved", "ss_scan_bwd_states_saved", "ss_step", "ss_conv1d_silu_fwd",
                     "ss_conv1d_silu_bwd", "ss_scan_bwd_noalloc",
                     "ss_scan_bwd_noalloc_max_scratch", "ss_xproj", "ss_xproj_wait_failures",
                     "ss_check_device_errors", "ss_debug_xproj_stuck_wait")
@@ -165,15 +168,25 @@ def _check_scan_inputs(u, delta, A, B, C, D, z, delta_bias):
 
 
 def ss_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
-                return_last_state=False, out=None, h_last=None, h0=None):
+                return_last_state=False, out=None, h_last=None, h0=None, save_to=None):
     """Forward selective scan on the current CUDA stream; returns y (and the
     final state when return_last_state).  ``h0``: float32 [Bsz][Dch][N]
-    state to start from (ss_scan_fwd_from_state); ``h_last`` may be ``h0``."""
+    state to start from (ss_scan_fwd_from_state); ``h_last`` may be ``h0``.
+    ``save_to``: a backward workspace (uint8 CUDA tensor) that also receives
+    the chunk states (ss_scan_fwd_save), for ss_scan_bwd(..., saved=True)."""
     Bsz, Dch, L, N = _check_scan_inputs(u, delta, A, B, C, D, z, delta_bias)
     y = torch.empty_like(u) if out is None else out
     if return_last_state and h_last is None:
         h_last = torch.empty((Bsz, Dch, N), device=u.device, dtype=torch.float32)
-    if h0 is None:
+    if save_to is not None:
+        if h0 is not None:
+            raise ValueError("save_to: the backward covers the zero initial state only")
+        st = _lib.ss_scan_fwd_save(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                   _ptr(z), _ptr(delta_bias), int(bool(softplus)), Bsz, Dch, L, N,
+                                   _dtype_code(u), _ptr(y), _ptr(h_last), _ptr(save_to),
+                                   save_to.numel(), _stream(u.device))
+        _check("ss_scan_fwd_save", st)
+    elif h0 is None:
         st = _lib.ss_scan_fwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
                               _ptr(delta_bias), int(bool(softplus)), Bsz, Dch, L, N,
                               _dtype_code(u), _ptr(y), _ptr(h_last), _stream(u.device))
@@ -196,13 +209,15 @@ def ss_scan_bwd_workspace_size(Bsz, Dch, L, N=N_STATE, dtype=SS_F32) -> int:
 
 
 def ss_scan_bwd(u, delta, A, B, C, D, z, delta_bias, softplus, dy, workspace=None, out=None,
-                stages=("ss_scan_bwd",)):
+                stages=("ss_scan_bwd",), saved=False):
     """Backward of ss_scan_fwd.  Returns dict du, ddelta, dA, dB, dC, dD, dz,
     ddelta_bias (None for absent optional inputs).  ``workspace``: optional
     uint8 CUDA tensor of at least ss_scan_bwd_workspace_size bytes.
     ``stages``: the C entry points to call in order (default the whole
     backward; ("ss_scan_bwd_states", "ss_scan_bwd_reverse", "ss_scan_bwd_reduce")
-    is equivalent, one stage per call)."""
+    is equivalent, one stage per call).  ``saved``: the workspace holds the
+    chunk states ss_scan_fwd(..., save_to=workspace) wrote for these inputs;
+    the whole backward and its first stage then use the _saved entry points."""
     Bsz, Dch, L, N = _check_scan_inputs(u, delta, A, B, C, D, z, delta_bias)
     _same(dy, (Bsz, Dch, L), u.dtype, "dy")
     dev = u.device
@@ -224,10 +239,14 @@ def ss_scan_bwd(u, delta, A, B, C, D, z, delta_bias, softplus, dy, workspace=Non
             _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]),
             _ptr(g["dz"]), _ptr(g["ddelta_bias"]), _ptr(workspace), workspace.numel(),
             _stream(dev))
+    if saved and workspace is None:
+        raise ValueError("saved=True needs the workspace ss_scan_fwd saved to")
     for name in stages:
         if name not in ("ss_scan_bwd", "ss_scan_bwd_states", "ss_scan_bwd_reverse",
                         "ss_scan_bwd_reduce"):
             raise ValueError(name)
+        if saved and name in ("ss_scan_bwd", "ss_scan_bwd_states"):
+            name += "_saved"
         _check(name, getattr(_lib, name)(*args))
     return g
 

@@ -61,10 +61,12 @@ int ss_version(void) { return 10000; }
 
 namespace {
 
+// ws non-null: also the chunk states, into the backward's workspace.
 ss_status run_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
                   const float* D, const void* z, const float* delta_bias, int softplus,
                   const float* h0, int64_t Bsz, int64_t Dch, int64_t L, int64_t N, ss_dtype dtype,
-                  void* y, float* h_last, ss_stream_t stream) {
+                  void* y, float* h_last, ss_stream_t stream, void* ws = nullptr,
+                  size_t ws_bytes = 0, bool save = false) {
   if (!known_dtype(dtype)) return SS_ERR_DTYPE;
   if (bad_size(Bsz) || bad_size(Dch) || bad_size(L) || bad_size(N)) return SS_ERR_SHAPE;
   if (Bsz > 65535 || product_too_big(Bsz, Dch, L)) return SS_ERR_SHAPE;
@@ -75,6 +77,10 @@ ss_status run_fwd(const void* u, const void* delta, const float* A, const void* 
       misaligned(D) || misaligned(z) || misaligned(delta_bias) || misaligned(y) ||
       misaligned(h_last) || misaligned(h0))
     return SS_ERR_ALIGN;
+  if (save && work) {
+    const size_t need = selscan::bwd_workspace_bytes(Bsz, Dch, L, N);
+    if (!ws || misaligned(ws) || ws_bytes < need) return SS_ERR_WORKSPACE;
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (!work) {
     if (h_last && Bsz > 0 && Dch > 0) {
@@ -87,7 +93,19 @@ ss_status run_fwd(const void* u, const void* delta, const float* A, const void* 
   }
   selscan::ScanArgs a{u, delta, A, B, C, D, z, delta_bias, softplus ? 1 : 0,
                       Bsz, Dch, L, to_dt(dtype), h0, (int)N};
-  return cuda_status(selscan::launch_scan_fwd(a, y, h_last, s));
+  if (!save) return cuda_status(selscan::launch_scan_fwd(a, y, h_last, s));
+  float* hc = reinterpret_cast<float*>(static_cast<char*>(ws) +
+                                       selscan::bwd_chunk_states_offset(Bsz, Dch, L, N));
+  cudaError_t e = selscan::launch_scan_fwd(a, y, h_last, s, hc);
+  if (e == cudaErrorNotSupported) {
+    // a chunked forward kernel: the backward's state summaries write them
+    e = selscan::launch_scan_fwd(a, y, h_last, s);
+    if (e == cudaSuccess) {
+      selscan::BwdOut none{};
+      e = selscan::launch_scan_bwd(selscan::kBwdChunkStates, a, none, ws, s);
+    }
+  }
+  return cuda_status(e);
 }
 
 }  // namespace
@@ -98,6 +116,15 @@ ss_status ss_scan_fwd(const void* u, const void* delta, const float* A, const vo
                       ss_dtype dtype, void* y, float* h_last, ss_stream_t stream) {
   return run_fwd(u, delta, A, B, C, D, z, delta_bias, softplus, nullptr, Bsz, Dch, L, N, dtype,
                  y, h_last, stream);
+}
+
+ss_status ss_scan_fwd_save(const void* u, const void* delta, const float* A, const void* B,
+                           const void* C, const float* D, const void* z,
+                           const float* delta_bias, int softplus, int64_t Bsz, int64_t Dch,
+                           int64_t L, int64_t N, ss_dtype dtype, void* y, float* h_last,
+                           void* workspace, size_t workspace_bytes, ss_stream_t stream) {
+  return run_fwd(u, delta, A, B, C, D, z, delta_bias, softplus, nullptr, Bsz, Dch, L, N, dtype,
+                 y, h_last, stream, workspace, workspace_bytes, true);
 }
 
 ss_status ss_scan_fwd_from_state(const void* u, const void* delta, const float* A,
@@ -170,8 +197,11 @@ ss_status zero_grads(int64_t Bsz, int64_t Dch, int64_t L, int64_t N, float* dA, 
   return cuda_status(e);
 }
 
-// phase < 0: all three stages in order; 0, 1, 2: one stage.
-ss_status run_bwd(int phase, const void* u, const void* delta, const float* A, const void* B,
+// phase < 0: all three stages in order; kBwdStates (or kBwdAdjointStates),
+// kBwdReverse, kBwdReduce: one stage.  saved: the chunk states are in the
+// workspace already (ss_scan_fwd_save), so the first stage computes the
+// adjoint carries only.
+ss_status run_bwd(int phase, bool saved, const void* u, const void* delta, const float* A, const void* B,
                   const void* C, const float* D, const void* z, const float* delta_bias,
                   int softplus, const void* dy, int64_t Bsz, int64_t Dch, int64_t L, int64_t N,
                   ss_dtype dtype, void* du, void* ddelta, float* dA, float* dB, float* dC,
@@ -184,7 +214,8 @@ ss_status run_bwd(int phase, const void* u, const void* delta, const float* A, c
   if (st != SS_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (!work) {
-    if (phase < 0 || phase == 2) return zero_grads(Bsz, Dch, L, N, dA, dB, dC, dD, ddelta_bias, s);
+    if (phase < 0 || phase == selscan::kBwdReduce)
+      return zero_grads(Bsz, Dch, L, N, dA, dB, dC, dD, ddelta_bias, s);
     return SS_OK;
   }
   selscan::ScanArgs a{u, delta, A, B, C, D, z, delta_bias, softplus ? 1 : 0,
@@ -192,7 +223,8 @@ ss_status run_bwd(int phase, const void* u, const void* delta, const float* A, c
   selscan::BwdOut o{dy, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias};
   for (int ph = 0; ph < 3; ++ph) {
     if (phase >= 0 && ph != phase) continue;
-    cudaError_t e = selscan::launch_scan_bwd(ph, a, o, workspace, s);
+    const int launch = (ph == selscan::kBwdStates && saved) ? selscan::kBwdAdjointStates : ph;
+    cudaError_t e = selscan::launch_scan_bwd(launch, a, o, workspace, s);
     if (e != cudaSuccess) return SS_ERR_CUDA;
   }
   return SS_OK;
@@ -222,10 +254,20 @@ __attribute__((visibility("hidden"))) ss_status selscan_check_bwd_args(
   u, delta, A, B, C, D, z, delta_bias, softplus, dy, Bsz, Dch, L, N, dtype, du, ddelta, dA, dB, \
       dC, dD, dz, ddelta_bias, workspace, workspace_bytes, stream
 
-ss_status ss_scan_bwd(SS_BWD_PARAMS) { return run_bwd(-1, SS_BWD_ARGS); }
-ss_status ss_scan_bwd_states(SS_BWD_PARAMS) { return run_bwd(0, SS_BWD_ARGS); }
-ss_status ss_scan_bwd_reverse(SS_BWD_PARAMS) { return run_bwd(1, SS_BWD_ARGS); }
-ss_status ss_scan_bwd_reduce(SS_BWD_PARAMS) { return run_bwd(2, SS_BWD_ARGS); }
+ss_status ss_scan_bwd(SS_BWD_PARAMS) { return run_bwd(-1, false, SS_BWD_ARGS); }
+ss_status ss_scan_bwd_states(SS_BWD_PARAMS) {
+  return run_bwd(selscan::kBwdStates, false, SS_BWD_ARGS);
+}
+ss_status ss_scan_bwd_reverse(SS_BWD_PARAMS) {
+  return run_bwd(selscan::kBwdReverse, false, SS_BWD_ARGS);
+}
+ss_status ss_scan_bwd_reduce(SS_BWD_PARAMS) {
+  return run_bwd(selscan::kBwdReduce, false, SS_BWD_ARGS);
+}
+ss_status ss_scan_bwd_saved(SS_BWD_PARAMS) { return run_bwd(-1, true, SS_BWD_ARGS); }
+ss_status ss_scan_bwd_states_saved(SS_BWD_PARAMS) {
+  return run_bwd(selscan::kBwdStates, true, SS_BWD_ARGS);
+}
 
 ss_status ss_step(float* h, const void* u_t, const void* delta_t, const float* A,
                   const void* B_t, const void* C_t, const float* D, const void* z_t,

@@ -54,12 +54,32 @@ struct StepArgs {
   int N = 16;  // state size: 8, 16, 32 or 64
 };
 
-// Forward: writes y and (if non-null) h_last.  Requires Bsz*Dch*L > 0.
-cudaError_t launch_scan_fwd(const ScanArgs& a, void* y, float* h_last, cudaStream_t s);
-
-// Backward workspace size (bytes) and the launch of one of its three stages
-// (phase 0: segment states, 1: reverse pass, 2: reduction of the partials).
+// Forward: writes y and (if non-null) h_last; with h_chunks non-null also the
+// state entering every kScanChunk-step chunk, [Bsz][Dch][chunk][N], when the
+// kernel the shape takes can (the row-sequential one); returns
+// cudaErrorNotSupported before launching anything when it cannot.
 // Requires Bsz*Dch*L > 0.
+cudaError_t launch_scan_fwd(const ScanArgs& a, void* y, float* h_last, cudaStream_t s,
+                            float* h_chunks = nullptr);
+
+// Chunk of the backward (steps), and of the forward's chunk states.
+constexpr int kScanChunk = 128;
+
+// Forward with chunk states: also writes, into the backward's workspace, the
+// state entering every kScanChunk-step chunk ([Bsz][Dch][chunk][N] fp32 at
+// bwd_chunk_states_offset), so that the backward need not recompute them.
+// Kernels that cannot write them run the backward's state summaries instead.
+size_t bwd_chunk_states_offset(int64_t Bsz, int64_t Dch, int64_t L, int64_t N);
+
+// Backward workspace size (bytes) and the launch of one of its stages.
+// Requires Bsz*Dch*L > 0.
+enum BwdPhase : int {
+  kBwdStates = 0,         // chunk states and adjoint carries (summaries + carries)
+  kBwdReverse = 1,        // the reverse pass
+  kBwdReduce = 2,         // fixed-order reduction of the partials
+  kBwdAdjointStates = 3,  // adjoint carries only: the chunk states are saved
+  kBwdChunkStates = 4,    // chunk states only (for the forward)
+};
 size_t bwd_workspace_bytes(int64_t Bsz, int64_t Dch, int64_t L, int64_t N);
 cudaError_t launch_scan_bwd(int phase, const ScanArgs& a, const BwdOut& o, void* ws,
                             cudaStream_t s);

@@ -46,6 +46,12 @@ namespace {
 constexpr int kKTb = 8;                    // steps per lane (main kernel)
 constexpr int kRLb = 16;                   // lanes per row
 constexpr int kBwdChunk = kKTb * kRLb;     // 128 steps per chunk
+static_assert(kBwdChunk == kScanChunk, "the forward's chunk states use the backward's chunks");
+
+// What the chunk-summary stage computes: both summaries; the state ones
+// alone (the chunk states for a forward that cannot write them); the adjoint
+// ones alone (the chunk states were saved by the forward).
+enum SumMode : int { kSumBoth = 0, kSumS = 1, kSumQ = 2 };
 constexpr int kRowBlock = 128;             // rows per CTA (main kernel)
 constexpr int kSumThreads = 128;           // rows per CTA (summary kernel)
 constexpr int kSumDepth = 3;               // input blocks in flight (summary kernel)
@@ -86,11 +92,13 @@ __device__ __forceinline__ float step_delta(float raw, float bias, int softplus)
 // NS states in groups of SG = min(NS, 16): grid z = NS / SG, each thread
 // holds the SG states of its group (states SG z .. SG z + SG - 1).
 // Registers capped for four CTAs per SM (128): 5% faster than three with
-// bf16 I/O, the same with fp32.
-template <typename Io, bool kVec, int NS>
+// bf16 I/O, the same with fp32.  MODE (SumMode) drops the state or the
+// adjoint summaries, their inputs and their stores.
+template <typename Io, bool kVec, int NS, int MODE>
 __global__ void __launch_bounds__(kSumThreads, 4)
     bwd_summary_kernel(ScanArgs p, BwdOut o, int64_t nrb, float* __restrict__ sumS,
                        float* __restrict__ sumQ, float* __restrict__ dsum_out) {
+  constexpr bool kS = MODE != kSumQ, kQ = MODE != kSumS;
   using T = typename Io::T;
   constexpr int CH = kBwdChunk;
   constexpr int SG = NS < 16 ? NS : 16;
@@ -112,12 +120,13 @@ __global__ void __launch_bounds__(kSumThreads, 4)
   // stage B, C of (b, chunk) transposed to [t][n]
   const T* Bb = static_cast<const T*>(p.B) + (b * NS + n0) * L;
   const T* Cb = static_cast<const T*>(p.C) + (b * NS + n0) * L;
-  for (int i = tid; i < 2 * SG * (CH / 8); i += kSumThreads) {
+  constexpr int w_lo = kS ? 0 : 1, w_hi = kQ ? 2 : 1;  // B (w = 0) and / or C (w = 1)
+  for (int i = tid; i < (w_hi - w_lo) * SG * (CH / 8); i += kSumThreads) {
     // consecutive threads -> consecutive states n: the transposed [t][n]
     // stores of a warp land in two 64-byte runs
     const int n = i % SG;
     const int wo = i / SG;
-    const int o = wo % (CH / 8), w = wo / (CH / 8);
+    const int o = wo % (CH / 8), w = w_lo + wo / (CH / 8);
     const T* src = (w ? Cb : Bb) + (int64_t)n * L + t0 + 8 * o;
     float v[8];
     load_kt<Io, 8, kVec>(src, 0, L - t0 - 8 * o, true, v);
@@ -132,10 +141,11 @@ __global__ void __launch_bounds__(kSumThreads, 4)
 #pragma unroll
   for (int n = 0; n < SG; ++n) A2[n] = p.A[d * NS + n0 + n] * kLog2e;
   const float bias = p.delta_bias ? p.delta_bias[d] : 0.f;
-  const T* urow = static_cast<const T*>(p.u) + row * L;
+  // the inputs a mode does not use are not read (they load as zeros)
+  const T* urow = kS ? static_cast<const T*>(p.u) + row * L : nullptr;
   const T* drow = static_cast<const T*>(p.delta) + row * L;
-  const T* zrow = p.z ? static_cast<const T*>(p.z) + row * L : nullptr;
-  const T* grow = static_cast<const T*>(o.dy) + row * L;
+  const T* zrow = (kQ && p.z) ? static_cast<const T*>(p.z) + row * L : nullptr;
+  const T* grow = kQ ? static_cast<const T*>(o.dy) + row * L : nullptr;
 
   float2 S[SG / 2], Q[SG / 2], cp[SG / 2];
 #pragma unroll
@@ -159,7 +169,7 @@ __global__ void __launch_bounds__(kSumThreads, 4)
         const int64_t t = t0 + tb + Io::kVec * v;
         const bool in = tb < CH && src[w] != nullptr && t < L;
         cp_async16(slot + (w * VPB + v) * kSumThreads + tid,
-                   in ? (const void*)(src[w] + t) : (const void*)urow, in ? 16 : 0);
+                   in ? (const void*)(src[w] + t) : (const void*)drow, in ? 16 : 0);
       }
   };
   if (kVec) {
@@ -192,33 +202,38 @@ __global__ void __launch_bounds__(kSumThreads, 4)
       for (int v = 0; v < VPB; ++v) r.w[v] = slot[(3 * VPB + v) * kSumThreads];
       decode_raw<Io, 8>(r, gg);
     } else {
-      load_kt<Io, 8, kVec>(urow, t, L, true, uu);
+      load_kt<Io, 8, kVec>(urow, t, L, urow != nullptr, uu);
       load_kt<Io, 8, kVec>(drow, t, L, true, dd);
       load_kt<Io, 8, kVec>(zrow, t, L, zrow != nullptr, zz);
-      load_kt<Io, 8, kVec>(grow, t, L, true, gg);
+      load_kt<Io, 8, kVec>(grow, t, L, grow != nullptr, gg);
     }
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
       const bool in = t + s < L;
       const float dt = in ? step_delta(dd[s], bias, p.softplus) : 0.f;
-      const float dtu = dt * uu[s];
-      const float yh = zrow ? gg[s] * zz[s] * sigmoid_f(zz[s]) : gg[s];
+      const float dtu = kS ? dt * uu[s] : 0.f;
+      const float yh = !kQ ? 0.f : (zrow ? gg[s] * zz[s] * sigmoid_f(zz[s]) : gg[s]);
       dsum += dt;
       const float4* bq = reinterpret_cast<const float4*>(sB + (tb + s) * SG);
       const float4* cq = reinterpret_cast<const float4*>(sC + (tb + s) * SG);
 #pragma unroll
       for (int k = 0; k < SG / 4; ++k) {
-        const float4 bv = bq[k], cv = cq[k];
+        const float4 bv = kS ? bq[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 cv = kQ ? cq[k] : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int q = 2 * k + h;
           const float2 e = mul2(make_float2(dt, dt), make_float2(A2[2 * q], A2[2 * q + 1]));
           const float2 a = make_float2(ex2f(e.x), ex2f(e.y));
-          const float2 bp = h ? make_float2(bv.z, bv.w) : make_float2(bv.x, bv.y);
-          const float2 cc = h ? make_float2(cv.z, cv.w) : make_float2(cv.x, cv.y);
-          S[q] = fma2(a, S[q], mul2(make_float2(dtu, dtu), bp));
-          cp[q] = mul2(cp[q], a);
-          Q[q] = fma2(cp[q], mul2(make_float2(yh, yh), cc), Q[q]);
+          if (kS) {
+            const float2 bp = h ? make_float2(bv.z, bv.w) : make_float2(bv.x, bv.y);
+            S[q] = fma2(a, S[q], mul2(make_float2(dtu, dtu), bp));
+          }
+          if (kQ) {
+            const float2 cc = h ? make_float2(cv.z, cv.w) : make_float2(cv.x, cv.y);
+            cp[q] = mul2(cp[q], a);
+            Q[q] = fma2(cp[q], mul2(make_float2(yh, yh), cc), Q[q]);
+          }
         }
       }
     }
@@ -228,8 +243,8 @@ __global__ void __launch_bounds__(kSumThreads, 4)
   float4* qo = reinterpret_cast<float4*>(sumQ + rc * NS + n0);
 #pragma unroll
   for (int k = 0; k < SG / 4; ++k) {
-    so[k] = make_float4(S[2 * k].x, S[2 * k].y, S[2 * k + 1].x, S[2 * k + 1].y);
-    qo[k] = make_float4(Q[2 * k].x, Q[2 * k].y, Q[2 * k + 1].x, Q[2 * k + 1].y);
+    if (kS) so[k] = make_float4(S[2 * k].x, S[2 * k].y, S[2 * k + 1].x, S[2 * k + 1].y);
+    if (kQ) qo[k] = make_float4(Q[2 * k].x, Q[2 * k].y, Q[2 * k + 1].x, Q[2 * k + 1].y);
   }
   if (n0 == 0) dsum_out[rc] = dsum;
 }
@@ -238,7 +253,7 @@ __global__ void __launch_bounds__(kSumThreads, 4)
 // 0b. chunk carries: sumS[row][c] <- h entering chunk c; sumQ[row][c] <- the
 //     adjoint carry entering chunk c from chunk c+1 (zero for the last).
 // ---------------------------------------------------------------------------
-template <int NS>
+template <int NS, int MODE>
 __global__ void bwd_carry_kernel(const float* __restrict__ A, int64_t Bsz, int64_t Dch,
                                  int64_t nch, float* __restrict__ sumS, float* __restrict__ sumQ,
                                  const float* __restrict__ dsum) {
@@ -249,7 +264,7 @@ __global__ void bwd_carry_kernel(const float* __restrict__ A, int64_t Bsz, int64
   const int64_t d = row % Dch;
   const float a2 = A[d * NS + n] * kLog2e;
   float h = 0.f;
-  for (int64_t c = 0; c < nch; ++c) {
+  for (int64_t c = 0; c < nch && MODE != kSumQ; ++c) {
     const size_t rc = (size_t)row * nch + c;
     const float P = ex2f(a2 * dsum[rc]);
     const float s = sumS[rc * NS + n];
@@ -257,7 +272,7 @@ __global__ void bwd_carry_kernel(const float* __restrict__ A, int64_t Bsz, int64
     h = fmaf(P, h, s);
   }
   float rho = 0.f;
-  for (int64_t c = nch - 1; c >= 0; --c) {
+  for (int64_t c = nch - 1; c >= 0 && MODE != kSumS; --c) {
     const size_t rc = (size_t)row * nch + c;
     const float P = ex2f(a2 * dsum[rc]);
     const float qv = sumQ[rc * NS + n];
@@ -799,23 +814,29 @@ cudaError_t launch_bwd_t(int phase, const ScanArgs& a, const BwdOut& o, void* ws
   float* pD = reinterpret_cast<float*>(base + w.pd);
   float* pbias = reinterpret_cast<float*>(base + w.pbias);
   cudaError_t e;
-  if (phase == 0) {
+  if (phase == kBwdStates || phase == kBwdAdjointStates || phase == kBwdChunkStates) {
     constexpr int SG = NS < 16 ? NS : 16;  // states per summary thread
     const int64_t nrb = (a.Dch + kSumThreads - 1) / kSumThreads;
     dim3 grid((unsigned)(nrb * w.nchunks), (unsigned)a.Bsz, (unsigned)(NS / SG));
     const size_t smem = sizeof(float) * 2 * kBwdChunk * SG +
                         (kVec ? sizeof(uint4) * kSumDepth * 4 * (8 / Io::kVec) * kSumThreads : 0);
-    auto kern = bwd_summary_kernel<Io, kVec, NS>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, kSumThreads, smem, s>>>(a, o, nrb, sumS, sumQ, dsum);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t n = a.Bsz * a.Dch * NS;
-    bwd_carry_kernel<NS><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a.A, a.Bsz, a.Dch,
-                                                                     w.nchunks, sumS, sumQ, dsum);
-    return cudaGetLastError();
+    const dim3 cgrid((unsigned)((n + 255) / 256));
+    auto run = [&](auto kern, auto carry) -> cudaError_t {
+      cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (r != cudaSuccess) return r;
+      kern<<<grid, kSumThreads, smem, s>>>(a, o, nrb, sumS, sumQ, dsum);
+      if ((r = cudaGetLastError()) != cudaSuccess) return r;
+      carry<<<cgrid, 256, 0, s>>>(a.A, a.Bsz, a.Dch, w.nchunks, sumS, sumQ, dsum);
+      return cudaGetLastError();
+    };
+    if (phase == kBwdStates)
+      return run(bwd_summary_kernel<Io, kVec, NS, kSumBoth>, bwd_carry_kernel<NS, kSumBoth>);
+    if (phase == kBwdAdjointStates)
+      return run(bwd_summary_kernel<Io, kVec, NS, kSumQ>, bwd_carry_kernel<NS, kSumQ>);
+    return run(bwd_summary_kernel<Io, kVec, NS, kSumS>, bwd_carry_kernel<NS, kSumS>);
   }
-  if (phase == 1) {
+  if (phase == kBwdReverse) {
     // 16-bit I/O: 4 warps per CTA, registers capped for three CTAs per SM
     // (168 used), one dB/dC slot buffer so that three CTAs also fit in
     // shared memory with 16 states: 12 warps per SM (measured fastest of
@@ -860,6 +881,10 @@ cudaError_t launch_bwd_io(int phase, const ScanArgs& a, const BwdOut& o, void* w
 
 size_t bwd_workspace_bytes(int64_t Bsz, int64_t Dch, int64_t L, int64_t N) {
   return ws_layout(Bsz, Dch, L, N).total;
+}
+
+size_t bwd_chunk_states_offset(int64_t Bsz, int64_t Dch, int64_t L, int64_t N) {
+  return ws_layout(Bsz, Dch, L, N).sumS;  // after the carries: h entering each chunk
 }
 
 cudaError_t launch_scan_bwd(int phase, const ScanArgs& a, const BwdOut& o, void* ws,

@@ -354,9 +354,11 @@ __device__ __forceinline__ void lds_states(const float* p, float2 (&v)[SPL / 2])
   }
 }
 
-template <typename Io, int R, int T, int NR, int NS, bool kVec>
+template <typename Io, int R, int T, int NR, int NS, bool kVec, bool kSave>
 __global__ void __launch_bounds__(4 * R / NR)
-    scan_fwd_rows_kernel(ScanArgs p, typename Io::T* __restrict__ y_out, float* __restrict__ h_last) {
+    scan_fwd_rows_kernel(ScanArgs p, typename Io::T* __restrict__ y_out, float* __restrict__ h_last,
+                         float* __restrict__ h_chunks) {
+  static_assert(kScanChunk % T == 0, "chunks of whole tiles");
   using E = typename Io::T;
   using Cfg = FwdRowsCfg<Io, R, T, NR, NS>;
   constexpr int NT = Cfg::NT, V = Cfg::V, VPR = Cfg::VPR, NV = Cfg::NV, SPL = Cfg::SPL;
@@ -560,6 +562,25 @@ __global__ void __launch_bounds__(4 * R / NR)
     __syncthreads();  // (dt, dt*u) and the B/C tile ready; phase C of tile i-1 done
 
     // ---- phase B of tile i
+    if (kSave && t0 % kScanChunk == 0) {
+      // the state entering chunk t0 / kScanChunk (the backward's chunk states)
+      const int64_t nch = (L + kScanChunk - 1) / kScanChunk, c = t0 / kScanChunk;
+#pragma unroll
+      for (int j = 0; j < NR; ++j) {
+        const int64_t qd = d0 + qr + j * (R / NR);
+        if (qd < Dch) {
+          float* dst = h_chunks + ((b * Dch + qd) * nch + c) * NS + SPL * qk;
+          if constexpr (SPL % 4 == 0) {
+#pragma unroll
+            for (int c4 = 0; c4 < SPL / 4; ++c4)
+              reinterpret_cast<float4*>(dst)[c4] = make_float4(
+                  h[j][2 * c4].x, h[j][2 * c4].y, h[j][2 * c4 + 1].x, h[j][2 * c4 + 1].y);
+          } else {
+            *reinterpret_cast<float2*>(dst) = h[j][0];
+          }
+        }
+      }
+    }
     {
       const float* Bq = Bf + SPL * qk;
       const float* Cq = Cf + SPL * qk;
@@ -615,14 +636,16 @@ __global__ void __launch_bounds__(4 * R / NR)
 }
 
 template <typename Io, int R, int T, int NR, int NS, bool kVec>
-static cudaError_t launch_fwd_rows(const ScanArgs& a, void* y, float* h_last, cudaStream_t s) {
+static cudaError_t launch_fwd_rows(const ScanArgs& a, void* y, float* h_last, cudaStream_t s,
+                                   float* h_chunks) {
   using Cfg = FwdRowsCfg<Io, R, T, NR, NS>;
-  auto kern = scan_fwd_rows_kernel<Io, R, T, NR, NS, kVec>;
+  auto kern = h_chunks ? scan_fwd_rows_kernel<Io, R, T, NR, NS, kVec, true>
+                       : scan_fwd_rows_kernel<Io, R, T, NR, NS, kVec, false>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((a.Dch + R - 1) / R), (unsigned)a.Bsz);
-  kern<<<grid, Cfg::NT, Cfg::smem, s>>>(a, static_cast<typename Io::T*>(y), h_last);
+  kern<<<grid, Cfg::NT, Cfg::smem, s>>>(a, static_cast<typename Io::T*>(y), h_last, h_chunks);
   return cudaGetLastError();
 }
 
@@ -663,42 +686,48 @@ static cudaError_t launch_fwd_t(const ScanArgs& a, void* y, float* h_last, cudaS
 constexpr int64_t kRowsKernelMinRows = 8192;
 
 template <typename Io, int NS>
-static cudaError_t launch_fwd_ns(const ScanArgs& a, void* y, float* h_last, cudaStream_t s) {
-  if (a.L % Io::kVec == 0) return launch_fwd_rows<Io, 32, 32, 1, NS, true>(a, y, h_last, s);
-  return launch_fwd_rows<Io, 32, 32, 1, NS, false>(a, y, h_last, s);
+static cudaError_t launch_fwd_ns(const ScanArgs& a, void* y, float* h_last, cudaStream_t s,
+                                 float* hc) {
+  if (a.L % Io::kVec == 0) return launch_fwd_rows<Io, 32, 32, 1, NS, true>(a, y, h_last, s, hc);
+  return launch_fwd_rows<Io, 32, 32, 1, NS, false>(a, y, h_last, s, hc);
 }
 
 template <typename Io>
-static cudaError_t launch_fwd_other_n(const ScanArgs& a, void* y, float* h_last, cudaStream_t s) {
+static cudaError_t launch_fwd_other_n(const ScanArgs& a, void* y, float* h_last, cudaStream_t s,
+                                      float* hc) {
   switch (a.N) {
-    case 8: return launch_fwd_ns<Io, 8>(a, y, h_last, s);
-    case 32: return launch_fwd_ns<Io, 32>(a, y, h_last, s);
-    case 64: return launch_fwd_ns<Io, 64>(a, y, h_last, s);
+    case 8: return launch_fwd_ns<Io, 8>(a, y, h_last, s, hc);
+    case 32: return launch_fwd_ns<Io, 32>(a, y, h_last, s, hc);
+    case 64: return launch_fwd_ns<Io, 64>(a, y, h_last, s, hc);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_scan_fwd(const ScanArgs& a, void* y, float* h_last, cudaStream_t s) {
+cudaError_t launch_scan_fwd(const ScanArgs& a, void* y, float* h_last, cudaStream_t s,
+                            float* hc) {
   if (a.N != kN) {
-    if (a.dt == Dt::BF16) return launch_fwd_other_n<IoBf16>(a, y, h_last, s);
-    if (a.dt == Dt::F16) return launch_fwd_other_n<IoF16>(a, y, h_last, s);
-    return launch_fwd_other_n<IoF32>(a, y, h_last, s);
+    if (a.dt == Dt::BF16) return launch_fwd_other_n<IoBf16>(a, y, h_last, s, hc);
+    if (a.dt == Dt::F16) return launch_fwd_other_n<IoF16>(a, y, h_last, s, hc);
+    return launch_fwd_other_n<IoF32>(a, y, h_last, s, hc);
   }
   const bool many_rows = a.Bsz * a.Dch >= kRowsKernelMinRows;
+  // the chunked kernels cannot write the chunk states
+  const bool rows = many_rows && a.L % (a.dt == Dt::F32 ? IoF32::kVec : IoBf16::kVec) == 0;
+  if (hc && !rows) return cudaErrorNotSupported;
   if (a.dt == Dt::BF16) {
     if (a.L % IoBf16::kVec == 0)
-      return many_rows ? launch_fwd_rows<IoBf16, 32, 32, 1, 16, true>(a, y, h_last, s)
+      return many_rows ? launch_fwd_rows<IoBf16, 32, 32, 1, 16, true>(a, y, h_last, s, hc)
                        : launch_fwd_pair<IoBf16, 4, 16>(a, y, h_last, s);
     return launch_fwd_t<IoBf16, 8, false>(a, y, h_last, s);
   }
   if (a.dt == Dt::F16) {
     if (a.L % IoF16::kVec == 0)
-      return many_rows ? launch_fwd_rows<IoF16, 32, 32, 1, 16, true>(a, y, h_last, s)
+      return many_rows ? launch_fwd_rows<IoF16, 32, 32, 1, 16, true>(a, y, h_last, s, hc)
                        : launch_fwd_pair<IoF16, 4, 16>(a, y, h_last, s);
     return launch_fwd_t<IoF16, 8, false>(a, y, h_last, s);
   }
   if (a.L % IoF32::kVec == 0)
-    return many_rows ? launch_fwd_rows<IoF32, 32, 32, 2, 16, true>(a, y, h_last, s)
+    return many_rows ? launch_fwd_rows<IoF32, 32, 32, 2, 16, true>(a, y, h_last, s, hc)
                      : launch_fwd_pair<IoF32, 8, 8>(a, y, h_last, s);
   return launch_fwd_t<IoF32, 8, false>(a, y, h_last, s);
 }
