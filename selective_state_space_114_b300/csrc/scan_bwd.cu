@@ -26,7 +26,7 @@
 //  stage 0b  bwd_carry: per (row, state), a walk over the chunks turns the
 //            summaries into the true incoming state h_in[c] and the incoming
 //            adjoint carry rho_in[c] = a lam at the first step of chunk c+1.
-//  stage 1   bwd_main: per (batch, chunk, block of 128 rows): per state pair,
+//  stage 1   bwd_main: per (batch, chunk, block of 64 or 128 rows): per state pair,
 //            forward fold / 16-lane scan / replay for h, reverse fold / scan /
 //            replay for lam, and all products.  dB and dC are summed over the
 //            block's rows in shared memory (fixed order) and written as one
@@ -52,7 +52,15 @@ static_assert(kBwdChunk == kScanChunk, "the forward's chunk states use the backw
 // alone (the chunk states for a forward that cannot write them); the adjoint
 // ones alone (the chunk states were saved by the forward).
 enum SumMode : int { kSumBoth = 0, kSumS = 1, kSumQ = 2 };
-constexpr int kRowBlock = 128;             // rows per CTA (main kernel)
+// Rows per CTA of the main kernel (one dB/dC partial each).  16-bit I/O: 64,
+// so that the bench layer's 3072 CTAs fill 6.9 waves of three CTAs per SM
+// (128 rows: 3.5 waves, 5% slower with the tail); fp32 (two CTAs per SM,
+// more waves already): 128, which writes half the partials.
+constexpr int kRowBlockMin = 64;
+template <typename Io>
+__host__ __device__ constexpr int row_block() {
+  return std::is_same<Io, IoF32>::value ? 128 : 64;
+}
 constexpr int kSumThreads = 128;           // rows per CTA (summary kernel)
 constexpr int kSumDepth = 3;               // input blocks in flight (summary kernel)
 
@@ -66,7 +74,7 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_
 inline WsLayout ws_layout(int64_t Bsz, int64_t Dch, int64_t L, int64_t N) {
   WsLayout w;
   w.nchunks = (L + kBwdChunk - 1) / kBwdChunk;
-  w.blocks = (Dch + kRowBlock - 1) / kRowBlock;
+  w.blocks = (Dch + kRowBlockMin - 1) / kRowBlockMin;  // partials sized for the smallest block
   const size_t rc = (size_t)(Bsz * Dch) * w.nchunks;  // (row, chunk) pairs
   size_t off = 0;
   w.sumS = off;  off = align256(off + sizeof(float) * rc * N);
@@ -494,7 +502,8 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks)
   using T = typename Io::T;
   using Sm = MainSmem<W, T, kSlotBufs, NS>;
   constexpr int KT = kKTb, RL = kRLb, CH = kBwdChunk, R = 2 * W, NT = W * 32;
-  constexpr int kPasses = kRowBlock / R;
+  constexpr int RB = row_block<Io>();
+  constexpr int kPasses = RB / R;
   constexpr int SR = (int)Sm::slot_row;
   extern __shared__ float4 smem4[];
   char* sm = reinterpret_cast<char*>(smem4);
@@ -529,7 +538,7 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks)
     issue_raw_bc<Io, CH, NS>(Bb, Cb, L, t0, raw, tid, NT);
     cp_async_commit();
     {
-      const int64_t d = g * kRowBlock + r;
+      const int64_t d = g * RB + r;
       issue_row_inputs<Io, KT, NT>(p, o.dy, b * p.Dch + (d < p.Dch ? d : 0), d < p.Dch,
                                    t0 + KT * j, L, ins, tid);
     }
@@ -558,7 +567,7 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks)
 
 #pragma unroll 1
   for (int pass = 0; pass < kPasses; ++pass) {
-    const int64_t d0 = g * kRowBlock + pass * R;
+    const int64_t d0 = g * RB + pass * R;
     if (d0 >= p.Dch) break;  // uniform over the CTA
     const int64_t d = d0 + r;
     const bool valid = d < p.Dch;
@@ -803,8 +812,9 @@ cudaError_t launch_main(const ScanArgs& a, const BwdOut& o, const WsLayout& w, f
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sm::total);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)(w.blocks * w.nchunks), (unsigned)a.Bsz);
-  kern<<<grid, W * 32, Sm::total, s>>>(a, o, w.blocks, sumS, sumQ, pBC, pA, pD, pbias);
+  const int64_t nrb = (a.Dch + row_block<Io>() - 1) / row_block<Io>();
+  dim3 grid((unsigned)(nrb * w.nchunks), (unsigned)a.Bsz);
+  kern<<<grid, W * 32, Sm::total, s>>>(a, o, nrb, sumS, sumQ, pBC, pA, pD, pbias);
   return cudaGetLastError();
 }
 
@@ -856,7 +866,8 @@ cudaError_t launch_bwd_t(int phase, const ScanArgs& a, const BwdOut& o, void* ws
       return launch_main<Io, kVec, 4, 3, 1, NS, false>(a, o, w, sumS, sumQ, pBC, pA, pD, pbias, s);
   }
   const int64_t n = 2 * a.Bsz * NS * a.L;
-  bwd_reduce_bc_kernel<NS><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(pBC, w.blocks, a.Bsz,
+  const int64_t nrb = (a.Dch + row_block<Io>() - 1) / row_block<Io>();
+  bwd_reduce_bc_kernel<NS><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(pBC, nrb, a.Bsz,
                                                                          a.L, o.dB, o.dC);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   bwd_reduce_param_kernel<NS><<<(unsigned)a.Dch, kParamGroups * NS, 0, s>>>(
