@@ -273,26 +273,37 @@ def ss_step(h, u_t, delta_t, A, B_t, C_t, D=None, z_t=None, delta_bias=None, sof
 
 
 class SelectiveScanFn(torch.autograd.Function):
-    """Autograd wrapper: forward = ss_scan_fwd, backward = ss_scan_bwd
-    (recomputes the states; saves only the inputs)."""
+    """Autograd wrapper.  keep_chunk_states (default): forward =
+    ss_scan_fwd_save into a backward workspace kept until the backward, which
+    is ss_scan_bwd_saved (it recomputes every per-step state but not the
+    states at the 128-step chunk boundaries).  Otherwise forward =
+    ss_scan_fwd and backward = ss_scan_bwd, which keeps only the inputs."""
 
     @staticmethod
-    def forward(ctx, u, delta, A, B, C, D, z, delta_bias, softplus):
+    def forward(ctx, u, delta, A, B, C, D, z, delta_bias, softplus, keep_chunk_states=True):
         ctx.softplus = bool(softplus)
         ctx.save_for_backward(u, delta, A, B, C, D, z, delta_bias)
-        return ss_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus)
+        ctx.ws = None
+        if keep_chunk_states and u.numel() > 0:
+            Bsz, Dch, L = u.shape
+            n = ss_scan_bwd_workspace_size(Bsz, Dch, L, A.shape[1], _dtype_code(u))
+            ctx.ws = torch.empty(max(n, 1), device=u.device, dtype=torch.uint8)
+        return ss_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus, save_to=ctx.ws)
 
     @staticmethod
     def backward(ctx, dy):
         u, delta, A, B, C, D, z, delta_bias = ctx.saved_tensors
-        g = ss_scan_bwd(u, delta, A, B, C, D, z, delta_bias, ctx.softplus, dy.contiguous())
+        g = ss_scan_bwd(u, delta, A, B, C, D, z, delta_bias, ctx.softplus, dy.contiguous(),
+                        workspace=ctx.ws, saved=ctx.ws is not None)
+        ctx.ws = None
         return (g["du"], g["ddelta"], g["dA"], g["dB"].to(B.dtype), g["dC"].to(C.dtype),
-                g["dD"], g["dz"], g["ddelta_bias"], None)
+                g["dD"], g["dz"], g["ddelta_bias"], None, None)
 
 
-def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True):
+def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
+                   keep_chunk_states=True):
     """Differentiable selective scan (see SelectiveScanFn)."""
-    return SelectiveScanFn.apply(u, delta, A, B, C, D, z, delta_bias, softplus)
+    return SelectiveScanFn.apply(u, delta, A, B, C, D, z, delta_bias, softplus, keep_chunk_states)
 
 
 def ss_conv1d_silu(x, w, bias=None, silu=True, out=None):

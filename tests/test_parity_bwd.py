@@ -102,16 +102,29 @@ def test_workspace_too_small_writes_nothing():
         assert torch.all(v == 5.0), k
 
 
-def test_autograd_wrapper_matches_direct_call():
+@pytest.mark.parametrize("keep", [True, False])
+def test_autograd_wrapper_matches_direct_call(keep):
+    """selective_scan's gradients are bitwise those of the direct calls it
+    makes: ss_scan_fwd(save_to=ws) + ss_scan_bwd(saved=True) by default,
+    ss_scan_bwd alone with keep_chunk_states=False."""
     x = make_case("f32", 2, 16, 300, seed=25, with_dy=True)
     dy = x.pop("dy")
     xd = inputs_to_dev(x, "f32")
     leaves = {k: v.clone().requires_grad_(True) for k, v in xd.items()}
     y = ss.selective_scan(leaves["u"], leaves["delta"], leaves["A"], leaves["B"], leaves["C"],
-                          leaves["D"], leaves["z"], leaves["delta_bias"], True)
+                          leaves["D"], leaves["z"], leaves["delta_bias"], True,
+                          keep_chunk_states=keep)
     dyd = to_dev(dy, "f32")
     y.backward(dyd)
-    g = run_bwd(xd, dyd)
+    if keep:
+        ws = torch.empty(ss.ss_scan_bwd_workspace_size(2, 16, 300), device="cuda",
+                         dtype=torch.uint8)
+        args = (xd["u"], xd["delta"], xd["A"], xd["B"], xd["C"], xd["D"], xd["z"],
+                xd["delta_bias"], True)
+        ss.ss_scan_fwd(*args, save_to=ws)
+        g = ss.ss_scan_bwd(*args, dyd, workspace=ws, saved=True)
+    else:
+        g = run_bwd(xd, dyd)
     names = {"u": "du", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD", "z": "dz",
              "delta_bias": "ddelta_bias"}
     for k, gk in names.items():
