@@ -462,7 +462,7 @@ def _device_inputs(cfg, dev, seed, with_dy=False):
     and delta_bias from the host generator."""
     import torch
     Bsz, Dch, L, N = cfg["Bsz"], cfg["Dch"], cfg["L"], cfg["N"]
-    dtype = torch.bfloat16 if cfg["dtype"] == "bf16" else torch.float32
+    dtype = {"bf16": torch.bfloat16, "f16": torch.float16}.get(cfg["dtype"], torch.float32)
     gen = torch.Generator(device=dev)
     gen.manual_seed(seed)
 
@@ -625,13 +625,66 @@ def next_rows(ss, dev, seed, peaks):
     flops = 2 * Bsz * L * Dch * (R + 2 * N) + 2 * Bsz * L * R * Dch
     res["xproj"]["tensor_tflops"] = round(flops / (ms[2] * 1e-3) / 1e12, 2)
     res["xproj"]["device_errors"] = ss.ss_check_device_errors()
+    del x, g, u, grads, xo
+    res.update(scan_variants(ss, dev, seed, peaks))
     return res
 
 
-# The sources the headline step's kernels are built from: ncu traffic taken
-# on other versions of these files is not reported.
-# the sources each timed kernel is built from (its ncu figures hold while they
-# are unchanged)
+def scan_variants(ss, dev, seed, peaks):
+    """The scan's other configurations on the bench layer's shape (8 x 1536 x
+    2048), inputs larger than L2 timed back to back: state size 64 (forward,
+    and the backward with the chunk states kept by the forward), fp16 I/O
+    (forward), and a chunked prefill (the forward in 4 pieces of 512 steps,
+    each continuing from the state the previous piece left)."""
+    import torch
+    res = {}
+    base = synth.config(CFG_INDEX)
+    # state size 64
+    cfg = dict(base, N=64)
+    x, _ = _device_inputs(cfg, dev, seed + 11, with_dy=True)
+    Bsz, Dch, L, N = cfg["Bsz"], cfg["Dch"], cfg["L"], cfg["N"]
+    E = Bsz * Dch * L
+    a = (x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], True)
+    y, g = torch.empty_like(x["u"]), _grads(x, dev)
+    ws = torch.empty(ss.ss_scan_bwd_workspace_size(Bsz, Dch, L, N, ss.SS_BF16), device=dev,
+                     dtype=torch.uint8)
+    tf, tb = _timed_ms([lambda: ss.ss_scan_fwd(*a, out=y, save_to=ws),
+                        lambda: ss.ss_scan_bwd(*a, x["dy"], workspace=ws, out=g, saved=True)],
+                       10, dev)
+    res["state_size_64_fwd"] = {"ms": round(tf, 4), "gelem_s": round(E / tf / 1e6, 2),
+                                **_r(roofline(method_work("fwd", 2, Dch, N), E, tf, peaks))}
+    res["state_size_64_bwd"] = {"ms": round(tb, 4), "gelem_s": round(E / tb / 1e6, 2),
+                                **_r(roofline(method_work("bwd", 2, Dch, N), E, tb, peaks))}
+    del x, y, g, ws
+    # fp16 I/O and chunked prefill (16 states)
+    cfg = dict(base, dtype="f16")
+    x, _ = _device_inputs(cfg, dev, seed + 12)
+    Bsz, Dch, L, N = cfg["Bsz"], cfg["Dch"], cfg["L"], cfg["N"]
+    a = (x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], True)
+    y = torch.empty_like(x["u"])
+    (t16,) = _timed_ms([lambda: ss.ss_scan_fwd(*a, out=y)], 10, dev)
+    res["fp16_fwd"] = {"ms": round(t16, 4), "gelem_s": round(E / t16 / 1e6, 2),
+                       **_r(roofline(method_work("fwd", 2, Dch, N), E, t16, peaks))}
+    xb, _ = _device_inputs(base, dev, seed + 13)
+    pieces, P = 4, L // 4
+    parts = [{k: xb[k][..., i * P:(i + 1) * P].contiguous() for k in ("u", "delta", "z", "B", "C")}
+             for i in range(pieces)]
+    yp = [torch.empty_like(pp["u"]) for pp in parts]
+    h = torch.empty((Bsz, Dch, N), device=dev)
+
+    def prefill():
+        for i, pp in enumerate(parts):
+            ss.ss_scan_fwd(pp["u"], pp["delta"], xb["A"], pp["B"], pp["C"], xb["D"], pp["z"],
+                           xb["delta_bias"], True, out=yp[i], h_last=h, return_last_state=True,
+                           h0=h if i else None)
+    (tp,) = _timed_ms([prefill], 10, dev)
+    res["chunked_prefill_4x512"] = {"ms": round(tp, 4), "gelem_s": round(E / tp / 1e6, 2),
+                                    **_r(roofline(method_work("fwd", 2, Dch, N), E, tp, peaks))}
+    return res
+
+
+# The sources each timed kernel is built from: its ncu figures are reported
+# only while these files are unchanged.
 KERNEL_SOURCES = {"fwd": ("common.cuh", "launch.h", "scan_fwd.cu"),
                   "bwd_states": ("common.cuh", "launch.h", "scan_bwd.cu"),
                   "bwd_reverse": ("common.cuh", "launch.h", "scan_bwd.cu")}
