@@ -272,6 +272,42 @@ __device__ __forceinline__ void scan16_rev(float& P, float& S, int j) {
 }  // namespace selscan
 
 // ===========================================================================
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialization (launch_pdl), so that it may be
+// scheduled while the previous kernel of the stream finishes.  It starts
+// with pdl_wait, which waits for that kernel to complete and its memory to be
+// visible, and calls pdl_trigger once its main work is done, which lets the
+// next kernel be scheduled as this one drains.  Only launch latency and block
+// scheduling overlap, never a memory access; triggering at the end rather
+// than the start keeps the next kernel's blocks from occupying SMs while
+// this one still computes.
+// ===========================================================================
+namespace selscan {
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
+}  // namespace selscan
+
+// ===========================================================================
 // Building blocks of the paired-state kernels.
 //
 // Two states (n, n+1) travel together in a float2 and are updated by one

@@ -34,6 +34,7 @@ constexpr int kConvFwdThreads = 128;  // 128 x 2 vectors = a 2048-step bf16 row 
 template <typename Io, int K, bool kVec>
 __global__ void __launch_bounds__(kConvFwdThreads)
     conv_fwd_kernel(ConvArgs p, int64_t vecs_per_row) {
+  pdl_wait();
   using T = typename Io::T;
   constexpr int V = Io::kVec;
   const int64_t row = (int64_t)blockIdx.y + (int64_t)blockIdx.z * gridDim.y;
@@ -73,6 +74,7 @@ __global__ void __launch_bounds__(kConvFwdThreads)
     }
     store_kt<Io, V, kVec>(ur, v * V, L, true, out);
   }
+  pdl_trigger();  // the main work is done: the next kernel may be scheduled
 }
 
 // ---------------------------------------------------------------------------
@@ -83,6 +85,7 @@ __global__ void __launch_bounds__(kConvFwdThreads)
 // ---------------------------------------------------------------------------
 template <typename Io, int K, bool kVec>
 __global__ void __launch_bounds__(kConvThreads, 4) conv_bwd_kernel(ConvArgs p, ConvGrads o) {
+  pdl_wait();
   using T = typename Io::T;
   constexpr int V = Io::kVec;
   __shared__ float red[K + 1][kConvThreads];
@@ -185,6 +188,7 @@ __global__ void __launch_bounds__(kConvThreads, 4) conv_bwd_kernel(ConvArgs p, C
     else if (o.dbias)
       o.dbias[d] = r;
   }
+  pdl_trigger();  // the main work is done: the next kernel may be scheduled
 }
 
 template <typename Io, int K>
@@ -197,16 +201,17 @@ cudaError_t launch_conv_k(int phase, const ConvArgs& a, const ConvGrads& o, cuda
     dim3 grid((unsigned)((vpr + kConvFwdThreads * kConvVpt - 1) / (kConvFwdThreads * kConvVpt)),
               (unsigned)gy, (unsigned)gz);
     if (vec)
-      conv_fwd_kernel<Io, K, true><<<grid, kConvFwdThreads, 0, s>>>(a, vpr);
+      return launch_pdl(conv_fwd_kernel<Io, K, true>, grid, dim3(kConvFwdThreads), 0, s, a, vpr);
     else
-      conv_fwd_kernel<Io, K, false><<<grid, kConvFwdThreads, 0, s>>>(a, vpr);
+      return launch_pdl(conv_fwd_kernel<Io, K, false>, grid, dim3(kConvFwdThreads), 0, s, a, vpr);
   } else {
     if (vec)
-      conv_bwd_kernel<Io, K, true><<<(unsigned)a.Dch, kConvThreads, 0, s>>>(a, o);
+      return launch_pdl(conv_bwd_kernel<Io, K, true>, dim3((unsigned)a.Dch), dim3(kConvThreads), 0,
+                        s, a, o);
     else
-      conv_bwd_kernel<Io, K, false><<<(unsigned)a.Dch, kConvThreads, 0, s>>>(a, o);
+      return launch_pdl(conv_bwd_kernel<Io, K, false>, dim3((unsigned)a.Dch), dim3(kConvThreads), 0,
+                        s, a, o);
   }
-  return cudaGetLastError();
 }
 
 template <typename Io>

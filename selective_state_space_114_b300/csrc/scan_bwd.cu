@@ -106,6 +106,7 @@ template <typename Io, bool kVec, int NS, int MODE>
 __global__ void __launch_bounds__(kSumThreads, 4)
     bwd_summary_kernel(ScanArgs p, BwdOut o, int64_t nrb, float* __restrict__ sumS,
                        float* __restrict__ sumQ, float* __restrict__ dsum_out) {
+  pdl_wait();
   constexpr bool kS = MODE != kSumQ, kQ = MODE != kSumS;
   using T = typename Io::T;
   constexpr int CH = kBwdChunk;
@@ -252,6 +253,7 @@ __global__ void __launch_bounds__(kSumThreads, 4)
       }
     }
   }
+  pdl_trigger();  // the main work is done: the next kernel may be scheduled
   const size_t rc = (size_t)row * nch + c;
   float4* so = reinterpret_cast<float4*>(sumS + rc * NS + n0);
   float4* qo = reinterpret_cast<float4*>(sumQ + rc * NS + n0);
@@ -271,6 +273,7 @@ template <int NS, int MODE>
 __global__ void bwd_carry_kernel(const float* __restrict__ A, int64_t Bsz, int64_t Dch,
                                  int64_t nch, float* __restrict__ sumS, float* __restrict__ sumQ,
                                  const float* __restrict__ dsum) {
+  pdl_wait();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= Bsz * Dch * NS) return;
   const int64_t row = i / NS;
@@ -293,6 +296,7 @@ __global__ void bwd_carry_kernel(const float* __restrict__ A, int64_t Bsz, int64
     sumQ[rc * NS + n] = rho;
     rho = fmaf(P, rho, qv);
   }
+  pdl_trigger();  // the main work is done: the next kernel may be scheduled
 }
 
 // ---------------------------------------------------------------------------
@@ -499,6 +503,7 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks)
     bwd_main_kernel(ScanArgs p, BwdOut o, int64_t nrb, const float* __restrict__ Hin,
                     const float* __restrict__ Rin, float* __restrict__ pBC,
                     float* __restrict__ pA, float* __restrict__ pD, float* __restrict__ pbias) {
+  pdl_wait();
   using T = typename Io::T;
   using Sm = MainSmem<W, T, kSlotBufs, NS>;
   constexpr int KT = kKTb, RL = kRLb, CH = kBwdChunk, R = 2 * W, NT = W * 32;
@@ -727,6 +732,7 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks)
     }
   }
   __syncthreads();
+  pdl_trigger();  // the main work is done: the next kernel may be scheduled
   // this block's dB / dC partial for the chunk
   float* out = pBC + ((size_t)(b * nrb + g) * 2) * NS * L;
   for (int i = tid; i < 2 * NS * CH; i += NT) {
@@ -742,6 +748,7 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks)
 template <int NS>
 __global__ void bwd_reduce_bc_kernel(const float* __restrict__ pBC, int64_t nrb, int64_t Bsz,
                                      int64_t L, float* __restrict__ dB, float* __restrict__ dC) {
+  pdl_wait();
   const int64_t per = Bsz * NS * L;  // elements of dB (and of dC)
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= 2 * per) return;
@@ -750,6 +757,7 @@ __global__ void bwd_reduce_bc_kernel(const float* __restrict__ pBC, int64_t nrb,
   float acc = 0.f;
   for (int64_t g = 0; g < nrb; ++g) acc += pBC[((b * nrb + g) * 2 + wh) * NS * L + nt];
   (wh ? dC : dB)[e] = acc;
+  pdl_trigger();  // the main work is done: the next kernel may be scheduled
 }
 
 // One CTA per channel d.  Thread (g, n), g = 0..7, sums the chunk partials of
@@ -762,6 +770,7 @@ __global__ void __launch_bounds__(kParamGroups * NS)
                             const float* __restrict__ pbias, int64_t Bsz, int64_t Dch,
                             int64_t nch, float* __restrict__ dA, float* __restrict__ dD,
                             float* __restrict__ dbias) {
+  pdl_wait();
   __shared__ float sA[kParamGroups * NS], sD[kParamGroups], sB[kParamGroups];
   const int64_t d = blockIdx.x;
   const int tid = threadIdx.x, n = tid % NS, gq = tid / NS;
@@ -801,6 +810,7 @@ __global__ void __launch_bounds__(kParamGroups * NS)
     if (dD) dD[d] = t1;
     if (dbias) dbias[d] = t2;
   }
+  pdl_trigger();  // the main work is done: the next kernel may be scheduled
 }
 
 template <typename Io, bool kVec, int W, int kMinBlocks, int kSlotBufs, int NS, bool kKeepB>
@@ -814,8 +824,8 @@ cudaError_t launch_main(const ScanArgs& a, const BwdOut& o, const WsLayout& w, f
   if (e != cudaSuccess) return e;
   const int64_t nrb = (a.Dch + row_block<Io>() - 1) / row_block<Io>();
   dim3 grid((unsigned)(nrb * w.nchunks), (unsigned)a.Bsz);
-  kern<<<grid, W * 32, Sm::total, s>>>(a, o, nrb, sumS, sumQ, pBC, pA, pD, pbias);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(W * 32), Sm::total, s, a, o, nrb, sumS, sumQ, pBC, pA, pD,
+                    pbias);
 }
 
 template <typename Io, bool kVec, int NS>
@@ -841,10 +851,10 @@ cudaError_t launch_bwd_t(int phase, const ScanArgs& a, const BwdOut& o, void* ws
     auto run = [&](auto kern, auto carry) -> cudaError_t {
       cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (r != cudaSuccess) return r;
-      kern<<<grid, kSumThreads, smem, s>>>(a, o, nrb, sumS, sumQ, dsum);
-      if ((r = cudaGetLastError()) != cudaSuccess) return r;
-      carry<<<cgrid, 256, 0, s>>>(a.A, a.Bsz, a.Dch, w.nchunks, sumS, sumQ, dsum);
-      return cudaGetLastError();
+      r = launch_pdl(kern, grid, dim3(kSumThreads), smem, s, a, o, nrb, sumS, sumQ, dsum);
+      if (r != cudaSuccess) return r;
+      return launch_pdl(carry, cgrid, dim3(256), 0, s, a.A, a.Bsz, a.Dch, w.nchunks, sumS, sumQ,
+                        dsum);
     };
     if (phase == kBwdStates)
       return run(bwd_summary_kernel<Io, kVec, NS, kSumBoth>, bwd_carry_kernel<NS, kSumBoth>);
@@ -867,12 +877,12 @@ cudaError_t launch_bwd_t(int phase, const ScanArgs& a, const BwdOut& o, void* ws
   }
   const int64_t n = 2 * a.Bsz * NS * a.L;
   const int64_t nrb = (a.Dch + row_block<Io>() - 1) / row_block<Io>();
-  bwd_reduce_bc_kernel<NS><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(pBC, nrb, a.Bsz,
-                                                                         a.L, o.dB, o.dC);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bwd_reduce_param_kernel<NS><<<(unsigned)a.Dch, kParamGroups * NS, 0, s>>>(
-      pA, pD, pbias, a.Bsz, a.Dch, w.nchunks, o.dA, o.dD, o.ddelta_bias);
-  return cudaGetLastError();
+  e = launch_pdl(bwd_reduce_bc_kernel<NS>, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s,
+                 (const float*)pBC, nrb, a.Bsz, a.L, o.dB, o.dC);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(bwd_reduce_param_kernel<NS>, dim3((unsigned)a.Dch), dim3(kParamGroups * NS), 0,
+                    s, (const float*)pA, (const float*)pD, (const float*)pbias, a.Bsz, a.Dch,
+                    w.nchunks, o.dA, o.dD, o.ddelta_bias);
 }
 
 template <typename Io, int NS>

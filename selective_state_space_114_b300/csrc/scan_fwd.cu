@@ -27,6 +27,7 @@ namespace selscan {
 template <typename Io, int W, bool kVec>
 __global__ void __launch_bounds__(W * 32)
     scan_fwd_kernel(ScanArgs p, typename Io::T* __restrict__ y_out, float* __restrict__ h_last) {
+  pdl_wait();
   using T = typename Io::T;
   constexpr int R = 2 * W;
   constexpr int NT = W * 32;
@@ -121,6 +122,7 @@ __global__ void __launch_bounds__(W * 32)
     }
     store_seg<Io, kVec>(yrow, ts, L, valid, y);
   }
+  pdl_trigger();  // the main work is done: the next kernel may be scheduled
   if (h_last) {
     __syncthreads();
     if (valid) h_last[row * kN + j] = carry[(cur * R + r) * kN + j];
@@ -154,6 +156,7 @@ struct FwdPairCfg {
 template <typename Io, int W, int KT>
 __global__ void __launch_bounds__(W * 32)
     scan_fwd_pair_kernel(ScanArgs p, typename Io::T* __restrict__ y_out, float* __restrict__ h_last) {
+  pdl_wait();
   using T = typename Io::T;
   using Cfg = FwdPairCfg<Io, W, KT>;
   constexpr int RL = Cfg::RL, R = Cfg::R, NT = Cfg::NT, CH = Cfg::CH;
@@ -277,6 +280,7 @@ __global__ void __launch_bounds__(W * 32)
     store_kt<Io, KT, true>(yrow, ts, L, valid, y);
   }
   cp_async_wait_all();
+  pdl_trigger();  // the main work is done: the next kernel may be scheduled
   if (h_last) {
     __syncthreads();
     if (valid) h_last[row * kN + j] = carry[(cur * R + r) * kN + j];
@@ -359,6 +363,7 @@ __global__ void __launch_bounds__(4 * R / NR)
     scan_fwd_rows_kernel(ScanArgs p, typename Io::T* __restrict__ y_out, float* __restrict__ h_last,
                          float* __restrict__ h_chunks) {
   static_assert(kScanChunk % T == 0, "chunks of whole tiles");
+  pdl_wait();
   using E = typename Io::T;
   using Cfg = FwdRowsCfg<Io, R, T, NR, NS>;
   constexpr int NT = Cfg::NT, V = Cfg::V, VPR = Cfg::VPR, NV = Cfg::NV, SPL = Cfg::SPL;
@@ -622,6 +627,7 @@ __global__ void __launch_bounds__(4 * R / NR)
       }
     }
   }
+  pdl_trigger();  // the main work is done: the next kernel may be scheduled
   if (h_last) {
 #pragma unroll
     for (int j = 0; j < NR; ++j) {
@@ -645,8 +651,8 @@ static cudaError_t launch_fwd_rows(const ScanArgs& a, void* y, float* h_last, cu
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((a.Dch + R - 1) / R), (unsigned)a.Bsz);
-  kern<<<grid, Cfg::NT, Cfg::smem, s>>>(a, static_cast<typename Io::T*>(y), h_last, h_chunks);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(Cfg::NT), Cfg::smem, s, a, static_cast<typename Io::T*>(y),
+                    h_last, h_chunks);
 }
 
 template <typename Io, int W, int KT>
@@ -657,8 +663,8 @@ static cudaError_t launch_fwd_pair(const ScanArgs& a, void* y, float* h_last, cu
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((a.Dch + Cfg::R - 1) / Cfg::R), (unsigned)a.Bsz);
-  kern<<<grid, W * 32, Cfg::smem, s>>>(a, static_cast<typename Io::T*>(y), h_last);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(W * 32), Cfg::smem, s, a, static_cast<typename Io::T*>(y),
+                    h_last);
 }
 
 template <typename Io, int W, bool kVec>
@@ -669,8 +675,7 @@ static cudaError_t launch_fwd_t(const ScanArgs& a, void* y, float* h_last, cudaS
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((a.Dch + R - 1) / R), (unsigned)a.Bsz);
-  kern<<<grid, W * 32, smem, s>>>(a, static_cast<typename Io::T*>(y), h_last);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(W * 32), smem, s, a, static_cast<typename Io::T*>(y), h_last);
 }
 
 // Rows of 16-byte multiples: with at least 8192 rows (enough quads of lanes to

@@ -120,17 +120,7 @@ __global__ void __launch_bounds__(kStepThreads) step_kernel(StepArgs p) {
 // before it touches the state.
 template <typename Io, int NS>
 cudaError_t launch_step_ns(const StepArgs& a, const dim3& grid, cudaStream_t s) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(kStepThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, step_kernel<Io, NS>, a);
+  return launch_pdl(step_kernel<Io, NS>, grid, dim3(kStepThreads), 0, s, a);
 }
 
 template <typename Io>

@@ -268,6 +268,7 @@ __global__ void __launch_bounds__(kXpThreads, 2)
     xproj_kernel(XprojArgs p, int split, const __grid_constant__ CUtensorMap map_u,
                  const __grid_constant__ CUtensorMap map_wx,
                  const __grid_constant__ CUtensorMap map_d) {
+  pdl_wait();
   using T = typename Io::T;
   constexpr bool kBf16 = std::is_same<Io, IoBf16>::value;
   extern __shared__ __align__(1024) unsigned char xsm[];
@@ -498,6 +499,7 @@ __global__ void __launch_bounds__(kXpThreads, 2)
   }
   cp_async_wait_all();
   if (lane == 0) bulk_wait_all();  // the warp's delta stores are complete
+  pdl_trigger();  // the main work is done: the next kernel may be scheduled
 
   if (failed) {
     // wait (bounded) for everything this CTA issued, so that no copy writes
@@ -611,14 +613,15 @@ cudaError_t launch_xproj(const XprojArgs& a, cudaStream_t s) {
     e = cudaFuncSetAttribute(xproj_kernel<IoBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
-    xproj_kernel<IoBf16><<<grid, kXpThreads, smem, s>>>(a, (int)split, mu_, mwx, md);
+    return launch_pdl(xproj_kernel<IoBf16>, dim3(grid), dim3(kXpThreads), smem, s, a, (int)split,
+                      mu_, mwx, md);
   } else {
     e = cudaFuncSetAttribute(xproj_kernel<IoF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
-    xproj_kernel<IoF16><<<grid, kXpThreads, smem, s>>>(a, (int)split, mu_, mwx, md);
+    return launch_pdl(xproj_kernel<IoF16>, dim3(grid), dim3(kXpThreads), smem, s, a, (int)split,
+                      mu_, mwx, md);
   }
-  return cudaGetLastError();
 }
 
 cudaError_t xproj_wait_failures(int* out) {
