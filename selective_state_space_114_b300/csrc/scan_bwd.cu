@@ -100,10 +100,17 @@ __device__ __forceinline__ float step_delta(float raw, float bias, int softplus)
 // NS states in groups of SG = min(NS, 16): grid z = NS / SG, each thread
 // holds the SG states of its group (states SG z .. SG z + SG - 1).
 // Registers capped for four CTAs per SM (128): 5% faster than three with
-// bf16 I/O, the same with fp32.  MODE (SumMode) drops the state or the
-// adjoint summaries, their inputs and their stores.
+// bf16 I/O, the same with fp32.  The adjoint-only mode with 16-bit I/O fits
+// in 95 registers and runs five CTAs per SM (6 µs less on the Mamba-130M
+// layer; six gained nothing more).  MODE (SumMode) drops the state or the
+// adjoint summaries, their inputs, their shared-memory tile and their stores.
+template <typename Io, int MODE>
+constexpr int sum_min_blocks() {
+  return (MODE == kSumQ && sizeof(typename Io::T) == 2) ? 5 : 4;
+}
+
 template <typename Io, bool kVec, int NS, int MODE>
-__global__ void __launch_bounds__(kSumThreads, 4)
+__global__ void __launch_bounds__(kSumThreads, sum_min_blocks<Io, MODE>())
     bwd_summary_kernel(ScanArgs p, BwdOut o, int64_t nrb, float* __restrict__ sumS,
                        float* __restrict__ sumQ, float* __restrict__ dsum_out) {
   pdl_wait();
@@ -112,9 +119,10 @@ __global__ void __launch_bounds__(kSumThreads, 4)
   constexpr int CH = kBwdChunk;
   constexpr int SG = NS < 16 ? NS : 16;
   extern __shared__ float4 smem4[];
-  float* sB = reinterpret_cast<float*>(smem4);  // [t][n of the group]
-  float* sC = sB + CH * SG;                      // [t][n of the group]
-  uint4* ring = reinterpret_cast<uint4*>(sC + CH * SG);  // input ring (16-byte rows only)
+  // the B and / or C tiles the mode uses, [t][n of the group], then the ring
+  float* sB = reinterpret_cast<float*>(smem4);
+  float* sC = sB + (kS ? CH * SG : 0);
+  uint4* ring = reinterpret_cast<uint4*>(sC + (kQ ? CH * SG : 0));  // input ring (16-byte rows only)
   const int tid = threadIdx.x;
   const int n0 = SG * blockIdx.z;
   const int64_t c = blockIdx.x / nrb;
@@ -844,11 +852,15 @@ cudaError_t launch_bwd_t(int phase, const ScanArgs& a, const BwdOut& o, void* ws
     constexpr int SG = NS < 16 ? NS : 16;  // states per summary thread
     const int64_t nrb = (a.Dch + kSumThreads - 1) / kSumThreads;
     dim3 grid((unsigned)(nrb * w.nchunks), (unsigned)a.Bsz, (unsigned)(NS / SG));
-    const size_t smem = sizeof(float) * 2 * kBwdChunk * SG +
-                        (kVec ? sizeof(uint4) * kSumDepth * 4 * (8 / Io::kVec) * kSumThreads : 0);
+    // one B or C tile per summary the mode makes, plus the input ring
+    auto smem_for = [&](int tiles) {
+      return sizeof(float) * tiles * kBwdChunk * SG +
+             (kVec ? sizeof(uint4) * kSumDepth * 4 * (8 / Io::kVec) * kSumThreads : 0);
+    };
     const int64_t n = a.Bsz * a.Dch * NS;
     const dim3 cgrid((unsigned)((n + 255) / 256));
-    auto run = [&](auto kern, auto carry) -> cudaError_t {
+    auto run = [&](auto kern, auto carry, int tiles) -> cudaError_t {
+      const size_t smem = smem_for(tiles);
       cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (r != cudaSuccess) return r;
       r = launch_pdl(kern, grid, dim3(kSumThreads), smem, s, a, o, nrb, sumS, sumQ, dsum);
@@ -857,10 +869,10 @@ cudaError_t launch_bwd_t(int phase, const ScanArgs& a, const BwdOut& o, void* ws
                         dsum);
     };
     if (phase == kBwdStates)
-      return run(bwd_summary_kernel<Io, kVec, NS, kSumBoth>, bwd_carry_kernel<NS, kSumBoth>);
+      return run(bwd_summary_kernel<Io, kVec, NS, kSumBoth>, bwd_carry_kernel<NS, kSumBoth>, 2);
     if (phase == kBwdAdjointStates)
-      return run(bwd_summary_kernel<Io, kVec, NS, kSumQ>, bwd_carry_kernel<NS, kSumQ>);
-    return run(bwd_summary_kernel<Io, kVec, NS, kSumS>, bwd_carry_kernel<NS, kSumS>);
+      return run(bwd_summary_kernel<Io, kVec, NS, kSumQ>, bwd_carry_kernel<NS, kSumQ>, 1);
+    return run(bwd_summary_kernel<Io, kVec, NS, kSumS>, bwd_carry_kernel<NS, kSumS>, 1);
   }
   if (phase == kBwdReverse) {
     // 16-bit I/O: 4 warps per CTA, registers capped for three CTAs per SM

@@ -48,6 +48,8 @@ def test_tiny_config_f32():
     (1, 3, 1),
     (2, 9, 37),
     (2, 33, 600),
+    (2, 3, 2049),   # 17 chunks: the carry walk takes a second block of 16 chunks
+    (1, 6, 4500),   # 36 chunks: three blocks, the last one ragged
 ])
 def test_shapes(dtype, Bsz, Dch, L):
     x = make_case(dtype, Bsz, Dch, L, seed=200 + L + Dch, with_dy=True)

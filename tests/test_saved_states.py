@@ -40,6 +40,8 @@ def _args(xd):
     ("bf16", 2, 48, 384, 8),      # other state sizes: row-sequential at any row count
     ("f32", 1, 40, 200, 32),
     ("bf16", 1, 20, 136, 64),
+    ("bf16", 1, 16, 4500, 16),    # 36 chunks: the adjoint carry walks three blocks
+    ("f32", 1, 24, 2200, 16),     # chunked forward, 18 chunks: state and adjoint carries
 ])
 def test_saved_backward_matches_oracle_and_recompute(dtype, Bsz, Dch, L, N):
     x = make_case(dtype, Bsz, Dch, L, seed=900 + L + N, with_dy=True, N=N)
