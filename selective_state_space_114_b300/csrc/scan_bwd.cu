@@ -387,7 +387,7 @@ __device__ __forceinline__ int slot_swizzle(int j) { return 2 * ((j >> 1) & 1); 
 // (pre-gate output, sum lam B, sum A lam a h) in the row's registers, stores
 // the row's dB and dC terms of the pair at dB_lo / dC_lo (state 2q, state 2q+1
 // at +CH) and the lane's dA terms of the two states at dA_lo[0], dA_lo[RL].
-template <int KT, int RL, int CH, int NS, bool kKeepB>
+template <int KT, int RL, int CH, int NS, bool kKeepB, bool kSyncSlots>
 __device__ __forceinline__ void bwd_state_pair(
     int q, int j, int r, bool valid, const float* A2s, const float* Ars, const float* hin_row,
     const float* rin_row, const float4* Bp, const float4* Cp, const float (&dl)[KT],
@@ -480,6 +480,10 @@ __device__ __forceinline__ void bwd_state_pair(
       yacc2[2 * k + 1] = fma2(c1, h, yacc2[2 * k + 1]);
       bb[2 * k + 1] = mul2(yh2[2 * k + 1], h);
     }
+    // kSyncSlots (one slot buffer): the previous pair's cross-row sum must
+    // have read the slots before they are written again; waiting only here
+    // lets that sum overlap the folds, scans and forward replay above
+    if (kSyncSlots) __syncthreads();
     store_steps<KT>(dC_lo, bb, slot_swizzle(j));
 
     // reverse replay: lam_t and the products
@@ -654,7 +658,7 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks)
     for (int q = 0; q < NS / 2; ++q) {
       const int sb = kSlotBufs == 2 ? (q & 1) : 0;
       float* slot = my_slot0 + (size_t)sb * R * SR;
-      bwd_state_pair<KT, RL, CH, NS, kKeepB>(q, j, r, valid, A2s, Ars, hin_row, rin_row, Bp, Cp, dl, du2,
+      bwd_state_pair<KT, RL, CH, NS, kKeepB, kSlotBufs == 1>(q, j, r, valid, A2s, Ars, hin_row, rin_row, Bp, Cp, dl, du2,
                                      yh2, dsum, yacc2, s12, s22, slot, slot + 2 * CH,
                                      dAs + (r * NS + 2 * q) * RL + j);
 
@@ -676,7 +680,6 @@ __global__ void __launch_bounds__(W * 32, kMinBlocks)
         hi = add2(hi, make_float2(v.z, v.w));
         *ap = make_float4(lo.x, lo.y, hi.x, hi.y);
       }
-      if (kSlotBufs == 1) __syncthreads();  // the single slot buffer is free again
     }
 
     // per-time-step outputs
