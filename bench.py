@@ -684,18 +684,27 @@ def scan_variants(ss, dev, seed, peaks):
 
 
 # The sources each timed kernel is built from: its ncu figures are reported
-# only while these files are unchanged.
+# only while their code (comments and blank lines aside) is unchanged.
 KERNEL_SOURCES = {"fwd": ("common.cuh", "launch.h", "scan_fwd.cu"),
                   "bwd_states": ("common.cuh", "launch.h", "scan_bwd.cu"),
                   "bwd_reverse": ("common.cuh", "launch.h", "scan_bwd.cu")}
+
+
+def _code_only(text):
+    """C++ source without its comments and blank lines, runs of spaces in a
+    line collapsed to one."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(" ".join(l.split()) for l in text.splitlines() if l.strip())
 
 
 def csrc_digest(kernel):
     import hashlib
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
-        h.update(open(os.path.join(ROOT, "selective_state_space_114_b300", "csrc", name),
-                      "rb").read())
+        src = open(os.path.join(ROOT, "selective_state_space_114_b300", "csrc", name)).read()
+        h.update(_code_only(src).encode())
     return h.hexdigest()[:16]
 
 

@@ -313,11 +313,12 @@ __global__ void bwd_carry_kernel(const float* __restrict__ A, int64_t Bsz, int64
 // Lane layout: the two rows of a warp sit in adjacent lanes (lane = 2 j + rs,
 // j = 0..15 the time segment, rs the row), so the 128-bit reads of the B / C
 // pair layout, identical for both rows, are served once per lane pair.
-// Per state pair the lane runs: forward fold, 16-segment scan, replay (h_t,
-// qq_t = a_t h_{t-1}, pre-gate output, dC terms), reverse fold, scan, replay
-// (lam_t, dB terms, the du / ddelta sums over states, dA terms).  Every row
-// writes its dB / dC terms to its own slot; after a barrier the 256 threads
-// sum the 16 rows' slots into the block accumulator.
+// Per state pair the lane runs: forward and reverse folds and their
+// 16-segment scans (interleaved), the forward replay (h_t, qq_t = a_t h_{t-1},
+// pre-gate output, dC terms), the reverse replay (lam_t, dB terms, the du /
+// ddelta sums over states, dA terms).  Every row of a pass writes its dB / dC
+// terms to its own slot; after a barrier the CTA's threads sum the pass's
+// rows' slots into the block accumulator.
 // ---------------------------------------------------------------------------
 template <int W, typename T, int kSlotBufs, int NS>
 struct MainSmem {

@@ -54,3 +54,13 @@ def test_roofline_picks_the_slowest_resource():
     r = bench.roofline(dict(fp32=1, mufu=100, bytes=1.0), E, 1.0, p)  # MUFU dominates
     assert r["resource"] == "mufu"
     assert math.isclose(r["frac"], round(100 * E / 1e-3 / 1e12 / p.mufu_t, 4))
+
+
+def test_kernel_digest_ignores_comments_only():
+    """The ncu figures stay attached to a kernel while its code is unchanged:
+    comments and blank lines do not count, code does."""
+    src = "// header\nint f(int x) {  // trailing\n  /* block\n  comment */ return x + 1;\n}\n"
+    same = "int f(int x) {\n\n  return x + 1;   \n}\n// new note\n"
+    other = "int f(int x) {\n  return x + 2;\n}\n"
+    assert bench._code_only(src) == bench._code_only(same)
+    assert bench._code_only(src) != bench._code_only(other)
